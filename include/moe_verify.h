@@ -1,0 +1,224 @@
+/*
+ * moe_verify.h -- C ABI of libmoeverify.so: the MoE expert operation of a
+ * speculative-decoding verification pass on one NVIDIA GB300 (sm_103a).
+ *
+ * Source of the method: "Speculative Decoding for Mixture-of-Experts Models: Expert
+ * Bytes, Kernel Bandwidth and the Best Draft Length" (Lan), cited as [Lan] with the
+ * section, equation or appendix that defines each operation.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  * Ownership: the caller owns every buffer (device or host).  The library never
+ *    allocates or frees device memory; scratch comes from a caller-provided workspace
+ *    of moe_workspace_bytes() bytes.
+ *  * Pointers marked [dev] are device pointers, [host] host pointers.  Every device
+ *    buffer must be 16-byte aligned; weight and activation buffers must also be
+ *    contiguous row-major in the layouts stated below.
+ *  * Asynchrony: a call that takes a stream enqueues its kernels on that stream and
+ *    returns without synchronising.  The host-only calls and moe_last_device_error (which
+ *    synchronises the stream) are the exceptions.
+ *  * Errors: every call returns a moe_status_t.  Arguments are validated on the host
+ *    before anything is launched (MOE_ERR_ARG / MOE_ERR_UNSUPPORTED, nothing enqueued).
+ *    A failed launch returns MOE_ERR_CUDA.  Problems only the device can see (an expert
+ *    id outside [0, N), a pipeline wait that timed out) are recorded in the workspace and
+ *    read back with moe_last_device_error; the offending slots are skipped, never
+ *    dereferenced.  Nothing throws across the ABI.
+ *  * Threading: calls are re-entrant; calls that share a workspace must be ordered on
+ *    one stream.
+ */
+#ifndef MOE_VERIFY_H
+#define MOE_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Identical to cudaStream_t; NULL means the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *moe_stream_t;
+
+#define MOE_ABI_VERSION 1
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_ARG = 1,            /* null pointer, bad size or misaligned buffer */
+    MOE_ERR_UNSUPPORTED = 2,    /* sizes or dtypes outside the supported range */
+    MOE_ERR_CUDA = 3,           /* a CUDA runtime call or a launch failed */
+    MOE_ERR_WORKSPACE = 4,      /* workspace missing or smaller than moe_workspace_bytes() */
+    MOE_ERR_BAD_ID = 5,         /* (device) an expert id outside [0, N) was skipped */
+    MOE_ERR_DEVICE_TIMEOUT = 6  /* (device) a pipeline wait gave up after its time limit */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+
+/*
+ * One MoE layer [Lan, §1: N experts, each token routed to m of them].
+ *   d  hidden size; f  expert intermediate size; N  experts; m  experts per token.
+ *   w_dtype  dtype of the expert weights; x_dtype  dtype of the pass activations.
+ * Weight layouts (row-major, one contiguous block per expert, nn.Linear convention):
+ *   w_gate, w_up  [N, f, d];   w_down  [N, d, f].
+ * Supported: 1 <= m <= N <= 1024, d and f multiples of 64, d <= 8192, f <= 65536;
+ * (w_dtype, x_dtype) = (MOE_BF16, MOE_BF16) or (MOE_F32, MOE_F32).
+ */
+typedef struct {
+    int32_t d, f, N, m;
+    int32_t w_dtype, x_dtype;
+} moe_layer_t;
+
+/* Largest pass size (tokens per verification pass) the expert operation accepts. */
+#define MOE_MAX_PASS_TOKENS 16
+
+/* Returns MOE_ABI_VERSION. */
+int32_t moe_abi_version(void);
+
+/* Static description of a status code (never NULL). */
+const char *moe_status_str(moe_status_t status);
+
+/*
+ * Bytes of device workspace the expert-operation calls need for this layer and passes
+ * of up to n_max tokens.  The workspace holds the device error word; it must be zeroed
+ * once with moe_workspace_init before its first use.
+ */
+size_t moe_workspace_bytes(const moe_layer_t *layer, int32_t n_max);
+
+/* Zeroes the workspace [dev] (ws_bytes >= moe_workspace_bytes) on stream s. */
+moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t s);
+
+/*
+ * Top-m routing [Lan, §1 "Routing, union and reuse": the router selects a set of m of
+ * the N experts for each token; the MoE layer combines the m expert outputs with the
+ * router's gate weights].
+ *   logits [dev] fp32 [n, N]   router logits of the pass's n tokens.
+ *   ids    [dev] int32 [n, m]  out: the m experts with the largest logits, in order of
+ *                              descending logit; an equal logit goes to the lower id.
+ *   gates  [dev] fp32 [n, m]   out: renorm != 0 -> softmax over the m selected logits
+ *                              (the full softmax renormalised over the selected set);
+ *                              renorm == 0 -> the full softmax over all N logits.
+ * NaN logits are not supported: they rank below every number, and the ids stay distinct
+ * and inside [0, N).  Supported: 0 <= n, 1 <= m <= min(N, 32), N <= 1024.
+ * n == 0 enqueues nothing.
+ */
+moe_status_t moe_route_topm(const float *logits, int32_t n, int32_t N, int32_t m, int32_t renorm,
+                            int32_t *ids, float *gates, moe_stream_t s);
+
+/*
+ * Slot grouping by expert, a counting sort [Lan, §1: a deduplicating kernel groups the
+ * pass's tokens by expert; App. E "Engine changes": the deduplicating engine sorts rows by
+ * expert].  Slot s = t*m + j names expert ids[s].
+ *   ids            [dev] int32 [n*m]
+ *   num_distinct   [dev] int32 [1]            out: U, the distinct experts of the pass
+ *   expert_list    [dev] int32 [min(N, n*m)]  out: the U distinct ids, ascending
+ *   expert_offsets [dev] int32 [min(N, n*m)+1] out: slots of expert_list[u] are
+ *                                             slot_order[offsets[u] .. offsets[u+1])
+ *   slot_order     [dev] int32 [n*m]          out: slot indices grouped by expert,
+ *                                             ascending slot index within an expert
+ *   ws             [dev] workspace or NULL.   Ids outside [0, N) are left out of every
+ *                                             group; with a workspace they set
+ *                                             MOE_ERR_BAD_ID there.
+ * Supported: 1 <= n*m <= 4096, N <= 1024.  Entries past U are left unspecified.
+ */
+moe_status_t moe_group_slots(const int32_t *ids, int32_t n, int32_t m, int32_t N,
+                             int32_t *num_distinct, int32_t *expert_list, int32_t *expert_offsets,
+                             int32_t *slot_order, void *ws, moe_stream_t s);
+
+/*
+ * Per-slot expert operation [Lan, §1: a per-slot kernel multiplies each token by each
+ * of its selected experts separately, with one expert read per slot; it requests m*n*w
+ * expert bytes per pass], fused with the weighted combine of the MoE layer:
+ *   for every slot (t, j), e = ids[t, j]:
+ *     h = silu(W_gate[e] x_t) * (W_up[e] x_t),   silu(z) = z / (1 + exp(-z))
+ *     y_t += gates[t, j] * W_down[e] h
+ *   w_gate, w_up, w_down [dev] layer weights in the layouts of moe_layer_t.
+ *   x     [dev] [n, d] in layer->x_dtype.
+ *   ids   [dev] int32 [n, m];  gates [dev] fp32 [n, m].
+ *   y     [dev] fp32 [n, d]    accumulate == 0: y is overwritten; != 0: added to.
+ *   ws    [dev] workspace of ws_bytes >= moe_workspace_bytes(layer, n).
+ * Supported: 1 <= n <= MOE_MAX_PASS_TOKENS.  Summation order inside y is not fixed
+ * (results may differ in the last bits between runs).
+ */
+moe_status_t moe_expert_op_perslot(const moe_layer_t *layer, const void *w_gate, const void *w_up,
+                                   const void *w_down, const void *x, const int32_t *ids,
+                                   const float *gates, int32_t n, int32_t accumulate, float *y,
+                                   void *ws, size_t ws_bytes, moe_stream_t s);
+
+/*
+ * Deduplicating expert operation [Lan, §1: a deduplicating kernel groups the pass's
+ * tokens by expert and reads each distinct expert once; it requests w * X(n) expert bytes
+ * for a pass whose slots name X(n) distinct experts], fused with the same combine.  The
+ * grouping is the output of moe_group_slots on the same ids (it stays on the device; the
+ * host never reads U).  Every distinct expert's weights are streamed from memory once
+ * for all of its tokens.
+ *   gates [dev] fp32 [n, m];  num_distinct, expert_list, expert_offsets, slot_order [dev]
+ *   as written by moe_group_slots for this pass; other arguments as the per-slot call.
+ * Shared (always-on) experts run through this call with their own weight block: ids
+ * listing all of them for every token, gates of 1 and accumulate = 1.
+ */
+moe_status_t moe_expert_op_dedup(const moe_layer_t *layer, const void *w_gate, const void *w_up,
+                                 const void *w_down, const void *x, const float *gates, int32_t n,
+                                 const int32_t *num_distinct, const int32_t *expert_list,
+                                 const int32_t *expert_offsets, const int32_t *slot_order,
+                                 int32_t accumulate, float *y, void *ws, size_t ws_bytes,
+                                 moe_stream_t s);
+
+/*
+ * Requested bytes of one pass [Lan, §1 "Bytes": E_slot = m*n*w, E_dedup = w * X(n);
+ * §2 "Effective bandwidth": u_bar(n) = E_dedup / E_slot].  Host only.
+ *   ids_host [host] int32 [n*m].
+ *   out: expert_bytes w = 3*d*f*sizeof(weight); slot_bytes = n*m*w; dedup_bytes = U*w;
+ *        act_bytes = n*d*sizeof(x) + n*d*4 (activations read, output written; reported
+ *        apart and never part of E_slot, E_dedup or u_bar); U; ubar = U / (n*m).
+ * Returns MOE_ERR_BAD_ID if an id is outside [0, N).
+ */
+typedef struct {
+    uint64_t expert_bytes, slot_bytes, dedup_bytes, act_bytes;
+    int32_t n, m, U, reserved;
+    double ubar;
+} moe_pass_bytes_t;
+
+moe_status_t moe_pass_bytes(const moe_layer_t *layer, const int32_t *ids_host, int32_t n,
+                            moe_pass_bytes_t *out);
+
+/*
+ * Bandwidth report over pass sizes n = n_lo .. n_lo+count-1 [Lan, §2 "Effective
+ * bandwidth": beta_p(n) = requested expert bytes of kernel p over its time,
+ * r(n) = beta_dedup / beta_slot, u_bar(n) = E_dedup / E_slot; §3.1 eq. (6): the saving
+ * S(n) = t_slot(n) - t_dedup(n), and (7): dedup is faster exactly where u_bar < r;
+ * §2 "Testing the inputs": the crossover is the smallest n from which the saving stays
+ * positive].  Host only; all arrays [host] of length count.
+ *   slot_bytes, dedup_bytes  requested bytes summed over the passes timed at each n.
+ *   t_slot, t_dedup          the matching summed times (any unit; beta is bytes/unit).
+ *   out: beta_slot, beta_dedup, ubar, r, saving; *crossover = the crossover n, or -1.
+ */
+moe_status_t moe_bandwidth_report(int32_t n_lo, int32_t count, const double *slot_bytes,
+                                  const double *dedup_bytes, const double *t_slot,
+                                  const double *t_dedup, double *beta_slot, double *beta_dedup,
+                                  double *ubar, double *r, double *saving, int32_t *crossover);
+
+/*
+ * Expected distinct experts of n tokens under independent uniform routing,
+ * N * (1 - q^n) with q = 1 - m/N [Lan, §1, after MoESD].  Host only.
+ */
+double moe_expected_union(int32_t N, int32_t m, int32_t n);
+
+/*
+ * Best draft length under geometric acceptance [Lan, §1 "Speculative decoding": the
+ * throughput T_a(k) = G_a(k) / V(k) with G_a(k) = 1 + a + ... + a^k; k*(a) is the
+ * smallest maximiser over k = 0..kmax].  V [host] double [kmax+1], the step time of a
+ * step that drafts k tokens.  Returns k*, or -1 if a is outside [0, 1) or some V <= 0.
+ */
+int32_t moe_best_draft_length(const double *V, int32_t kmax, double a);
+
+/*
+ * Synchronises stream s, reads the device error word of the workspace [dev] into *code
+ * (a moe_status_t value; MOE_OK if nothing was recorded) and clears it.
+ */
+moe_status_t moe_last_device_error(void *ws, moe_stream_t s, int32_t *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_VERIFY_H */

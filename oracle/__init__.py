@@ -1,0 +1,231 @@
+"""CPU oracle for the MoE verify-pass expert operation (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` leg of ``bench.py``
+import this package.  The product library never loads it, and the two share no code.
+
+The arithmetic lives in ``moe_oracle.c`` (plain C, fp64 accumulation; every function
+cites the passage of "Speculative Decoding for Mixture-of-Experts Models" (Lan) it
+follows).  This module compiles it with gcc into ``oracle/_build/`` and wraps it with
+ctypes and numpy arrays.  Parity of every function here is pinned by
+``tests/test_oracle_pins.py``; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libmoe_oracle.so")
+
+F32, BF16 = 0, 1
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared object (gcc, -O2, no fast-math).  Returns its path."""
+    with _lock:
+        stale = (not os.path.exists(_LIB_PATH)) or (
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+        if force or stale:
+            os.makedirs(_BUILD, exist_ok=True)
+            tmp = _LIB_PATH + f".tmp{os.getpid()}"
+            subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-Wall", "-Wextra",
+                            "-o", tmp, _SRC, "-lm"], check=True)
+            os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P, I, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+        lib.oracle_route_topm.argtypes = [P, I, I, I, I, P, P]
+        lib.oracle_group_slots.argtypes = [P, I, I, I, P, P, P, P]
+        lib.oracle_expert_op_perslot.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, I, P]
+        lib.oracle_expert_op_dedup.argtypes = [I, I, I, I, I, I, P, P, P, P, P, I, I, P, P, P, P]
+        lib.oracle_expert_op_token.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, I, P]
+        lib.oracle_pass_bytes.argtypes = [I, I, I, I, I, I, P, I, P, P, P]
+        lib.oracle_union_size.argtypes = [P, I, I, I, I, I]
+        lib.oracle_reuse_estimate.argtypes = [P, I, I, I, I]
+        lib.oracle_reuse_estimate.restype = D
+        lib.oracle_expected_union.argtypes = [I, I, I]
+        lib.oracle_expected_union.restype = D
+        lib.oracle_expected_tokens.argtypes = [D, I]
+        lib.oracle_expected_tokens.restype = D
+        lib.oracle_best_draft_length.argtypes = [P, I, D]
+        lib.oracle_crossover.argtypes = [P, P, I, I]
+        lib.oracle_bandwidth_report.argtypes = [I, I, P, P, P, P, P, P, P, P, P, P]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def _wcode(a: np.ndarray) -> int:
+    """Weights/activations: float32 arrays are fp32, uint16 arrays hold bf16 bit patterns."""
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    raise TypeError(f"oracle takes float32 or bf16-as-uint16 arrays, got {a.dtype}")
+
+
+def route_topm(logits: np.ndarray, m: int, renorm: bool = True):
+    """Top-m routing: returns (ids int32 [n, m], gates float64 [n, m])."""
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    n, N = logits.shape
+    ids = np.zeros((n, m), np.int32)
+    gates = np.zeros((n, m), np.float64)
+    rc = _load().oracle_route_topm(_ptr(logits), n, N, m, int(bool(renorm)), _ptr(ids), _ptr(gates))
+    if rc != 0:
+        raise ValueError("oracle_route_topm: bad arguments or NaN logit")
+    return ids, gates
+
+
+def group_slots(ids: np.ndarray, N: int):
+    """Counting sort of slots by expert: returns (U, expert_list[U], offsets[U+1], order[n*m])."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    n, m = ids.shape
+    cap = min(N, n * m)
+    U = np.zeros(1, np.int32)
+    lst = np.zeros(max(cap, 1), np.int32)
+    off = np.zeros(cap + 1, np.int32)
+    order = np.zeros(max(n * m, 1), np.int32)
+    rc = _load().oracle_group_slots(_ptr(ids), n, m, N, _ptr(U), _ptr(lst), _ptr(off), _ptr(order))
+    if rc != 0:
+        raise ValueError("oracle_group_slots: expert id out of range")
+    u = int(U[0])
+    return u, lst[:u].copy(), off[:u + 1].copy(), order[:n * m].copy()
+
+
+def _check_layer(wg, wu, wd, x):
+    N, f, d = wg.shape
+    assert wu.shape == (N, f, d) and wd.shape == (N, d, f) and x.shape[1] == d
+    assert wg.dtype == wu.dtype == wd.dtype
+    return N, f, d
+
+
+def expert_op_perslot(wg, wu, wd, x, ids, gates):
+    """Per-slot expert op + combine.  Weights [N,f,d],[N,f,d],[N,d,f]; x [n,d].  Returns y float64 [n,d]."""
+    wg, wu, wd, x = (np.ascontiguousarray(a) for a in (wg, wu, wd, x))
+    N, f, d = _check_layer(wg, wu, wd, x)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    gates = np.ascontiguousarray(gates, dtype=np.float64)
+    n, m = ids.shape
+    y = np.zeros((n, d), np.float64)
+    rc = _load().oracle_expert_op_perslot(d, f, N, m, _wcode(wg), _wcode(x), _ptr(wg), _ptr(wu),
+                                          _ptr(wd), _ptr(x), _ptr(ids), _ptr(gates), n, _ptr(y))
+    if rc != 0:
+        raise ValueError("oracle_expert_op_perslot: expert id out of range")
+    return y
+
+
+def expert_op_dedup(wg, wu, wd, x, gates, m, grouping):
+    """Deduplicating expert op + combine over a grouping (U, list, offsets, order)."""
+    wg, wu, wd, x = (np.ascontiguousarray(a) for a in (wg, wu, wd, x))
+    N, f, d = _check_layer(wg, wu, wd, x)
+    gates = np.ascontiguousarray(gates, dtype=np.float64)
+    n = gates.shape[0]
+    U, lst, off, order = grouping
+    lst = np.ascontiguousarray(lst, dtype=np.int32)
+    off = np.ascontiguousarray(off, dtype=np.int32)
+    order = np.ascontiguousarray(order, dtype=np.int32)
+    y = np.zeros((n, d), np.float64)
+    rc = _load().oracle_expert_op_dedup(d, f, N, m, _wcode(wg), _wcode(x), _ptr(wg), _ptr(wu),
+                                        _ptr(wd), _ptr(x), _ptr(gates), n, int(U), _ptr(lst),
+                                        _ptr(off), _ptr(order), _ptr(y))
+    if rc != 0:
+        raise ValueError("oracle_expert_op_dedup: expert id out of range")
+    return y
+
+
+def expert_op_token(wg, wu, wd, x, ids, gates, t):
+    """Layer output of token t alone (for spot checks of large passes).  Returns float64 [d]."""
+    wg, wu, wd, x = (np.ascontiguousarray(a) for a in (wg, wu, wd, x))
+    N, f, d = _check_layer(wg, wu, wd, x)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    gates = np.ascontiguousarray(gates, dtype=np.float64)
+    m = ids.shape[1]
+    y = np.zeros(d, np.float64)
+    rc = _load().oracle_expert_op_token(d, f, N, m, _wcode(wg), _wcode(x), _ptr(wg), _ptr(wu),
+                                        _ptr(wd), _ptr(x), _ptr(ids), _ptr(gates), int(t), _ptr(y))
+    if rc != 0:
+        raise ValueError("oracle_expert_op_token: expert id out of range")
+    return y
+
+
+def pass_bytes(d, f, N, ids, w_dtype=BF16, x_dtype=BF16):
+    """Bytes of one pass: dict(expert_bytes, slot_bytes, dedup_bytes, act_bytes, U, ubar)."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    n, m = ids.shape
+    out = np.zeros(4, np.uint64)
+    U = np.zeros(1, np.int32)
+    ubar = np.zeros(1, np.float64)
+    rc = _load().oracle_pass_bytes(d, f, N, m, w_dtype, x_dtype, _ptr(ids), n, _ptr(out), _ptr(U), _ptr(ubar))
+    if rc != 0:
+        raise ValueError("oracle_pass_bytes: expert id out of range")
+    return dict(expert_bytes=int(out[0]), slot_bytes=int(out[1]), dedup_bytes=int(out[2]),
+                act_bytes=int(out[3]), U=int(U[0]), ubar=float(ubar[0]))
+
+
+def union_size(sets: np.ndarray, N: int, t0: int, n: int) -> int:
+    sets = np.ascontiguousarray(sets, dtype=np.int32)
+    T, m = sets.shape
+    r = _load().oracle_union_size(_ptr(sets), T, m, N, t0, n)
+    if r < 0:
+        raise ValueError("oracle_union_size: bad arguments")
+    return int(r)
+
+
+def reuse_estimate(sets: np.ndarray, N: int, n: int) -> float:
+    sets = np.ascontiguousarray(sets, dtype=np.int32)
+    T, m = sets.shape
+    return float(_load().oracle_reuse_estimate(_ptr(sets), T, m, N, n))
+
+
+def expected_union(N: int, m: int, n: int) -> float:
+    return float(_load().oracle_expected_union(N, m, n))
+
+
+def expected_tokens(a: float, k: int) -> float:
+    return float(_load().oracle_expected_tokens(float(a), int(k)))
+
+
+def best_draft_length(V, a: float) -> int:
+    V = np.ascontiguousarray(V, dtype=np.float64)
+    return int(_load().oracle_best_draft_length(_ptr(V), len(V) - 1, float(a)))
+
+
+def crossover(t_slot, t_dedup, n_lo: int):
+    """Smallest n from which t_slot - t_dedup stays positive, or None."""
+    t_slot = np.ascontiguousarray(t_slot, dtype=np.float64)
+    t_dedup = np.ascontiguousarray(t_dedup, dtype=np.float64)
+    n_hi = n_lo + len(t_slot) - 1
+    r = _load().oracle_crossover(_ptr(t_slot), _ptr(t_dedup), n_lo, n_hi)
+    return None if r < 0 else int(r)
+
+
+def bandwidth_report(n_lo, slot_bytes, dedup_bytes, t_slot, t_dedup):
+    """dict of beta_slot, beta_dedup, ubar, r, saving (arrays) and crossover (int or None)."""
+    arrs = [np.ascontiguousarray(a, dtype=np.float64) for a in (slot_bytes, dedup_bytes, t_slot, t_dedup)]
+    count = len(arrs[0])
+    outs = [np.zeros(count, np.float64) for _ in range(5)]
+    cross = np.zeros(1, np.int32)
+    rc = _load().oracle_bandwidth_report(int(n_lo), count, *[_ptr(a) for a in arrs],
+                                         *[_ptr(o) for o in outs], _ptr(cross))
+    if rc != 0:
+        raise ValueError("oracle_bandwidth_report: non-positive time or bytes")
+    res = dict(zip(("beta_slot", "beta_dedup", "ubar", "r", "saving"), outs))
+    res["crossover"] = None if cross[0] < 0 else int(cross[0])
+    return res
