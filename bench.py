@@ -1,0 +1,522 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE verify-pass expert operation on GB300.
+
+Metric: expert-operation µs per pass and achieved HBM TB/s on requested expert bytes,
+against the pass size n = 1..16, for the per-slot and the deduplicating forms.
+
+Workload (default): a 48-layer Qwen3-30B-A3B-shaped expert stack (d=2048, N=128 experts,
+top-8, f=768, bf16; 57.98 GB resident), per-layer seeded routing traces with reuse 0.4,
+one shared pass x for every layer.  One *step* is one verification pass at every
+n = 1..16 through all 48 layers in both forms:
+    route (top-m of the 48*n router logits, one launch)
+    per-slot pass   (48 expert launches)
+    grouping        (48 counting sorts)
+    dedup pass      (48 expert launches)
+Each (n, phase) is a CUDA graph of the library's own kernels; events between the phases
+give the per-form times.  The weights (58 GB) are far larger than L2, and the layers run
+one after another, so no pass finds its weights in L2 from a previous pass.
+
+value    = expert bytes requested by both forms in the step / step time (TB/s, decimal).
+e2e      = the same with the step's inputs copied from pinned host memory and the outputs
+           copied back inside the timed region.
+roofline = the expert kernel: requested bytes per launch / its mean launch time, against
+           the measured HBM copy bandwidth.
+
+--impl reference times the CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_speculative_decoding_gb300 import api, synth  # noqa: E402
+from moe_speculative_decoding_gb300 import build as mbuild  # noqa: E402
+from moe_speculative_decoding_gb300.configs import BY_NAME, QWEN3_STACK  # noqa: E402
+
+METRIC = "MoE verify-pass expert-op µs and achieved HBM TB/s vs pass size n=1..16"
+UNIT = "TB/s"
+A_GRID = [round(0.10 + 0.05 * i, 2) for i in range(18)]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default=QWEN3_STACK.name, choices=sorted(BY_NAME))
+    p.add_argument("--layers", type=int, default=None, help="override the stack depth (smaller test runs)")
+    p.add_argument("--n-max", type=int, default=None)
+    p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------- helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            return json.load(fh), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.rows = []
+        if self.proc is None:
+            return
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.strip().splitlines():
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def summary(self):
+        rows = getattr(self, "rows", [])
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch of a kernel from the committed ncu summary, when it was taken on
+    the current source of that kernel; None otherwise."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        data = json.load(fh)
+    ent = data.get(kernel)
+    if not ent:
+        return None
+    import hashlib
+    src = os.path.join(ROOT, ent["source"])
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if digest != ent.get("source_sha256"):
+        return None
+    return ent
+
+
+# --------------------------------------------------------------------- our arm
+
+class StackBench:
+    def __init__(self, wl, layers, n_values, windows, device, use_graph=True):
+        self.wl, self.L, self.n_values, self.windows, self.dev = wl, layers, n_values, windows, device
+        self.layer = api.make_layer(wl.d, wl.f, wl.N, wl.m, "bf16")
+        self.use_graph = use_graph
+        t0 = time.time()
+        self.weights = [synth.expert_weights(wl.N, wl.f, wl.d, torch.bfloat16,
+                                             synth.seed_for(wl.index, layer=l), device=device)
+                        for l in range(layers)]
+        torch.cuda.synchronize(device)
+        self.t_weights = time.time() - t0
+        T = windows * max(n_values)
+        self.sets, logits = synth.routing_traces(layers, T, wl.N, wl.m, wl.rhos[0],
+                                                 seed=synth.seed_for(wl.index, stream=2))
+        self.ws = api.workspace(self.layer, 16, device)
+        self.per_n = {}
+        for n in n_values:
+            lw = np.stack([logits[:, w * n:(w + 1) * n, :].reshape(layers * n, wl.N) for w in range(windows)])
+            xw = torch.stack([synth.activations(n, wl.d, torch.bfloat16,
+                                                synth.seed_for(wl.index, stream=1000 + 17 * n + w), device=device)
+                              for w in range(windows)])
+            st = dict(
+                logits_all=torch.from_numpy(np.ascontiguousarray(lw)).to(device),
+                x_all=xw.contiguous(),
+                logits=torch.empty((layers * n, wl.N), dtype=torch.float32, device=device),
+                x=torch.empty((n, wl.d), dtype=torch.bfloat16, device=device),
+                ids=torch.empty((layers * n, wl.m), dtype=torch.int32, device=device),
+                gates=torch.empty((layers * n, wl.m), dtype=torch.float32, device=device),
+                y_slot=torch.zeros((layers, n, wl.d), dtype=torch.float32, device=device),
+                y_dedup=torch.zeros((layers, n, wl.d), dtype=torch.float32, device=device),
+                groups=[api.Grouping.empty(n, wl.m, wl.N, device) for _ in range(layers)],
+            )
+            bytes_slot, bytes_dedup = [], []
+            for w in range(windows):
+                bs = bd = 0
+                for l in range(layers):
+                    pb = api.pass_bytes(self.layer, self.sets[l, w * n:(w + 1) * n])
+                    bs += pb["slot_bytes"]
+                    bd += pb["dedup_bytes"]
+                bytes_slot.append(bs)
+                bytes_dedup.append(bd)
+            st["bytes_slot"], st["bytes_dedup"] = bytes_slot, bytes_dedup
+            self.per_n[n] = st
+        self.graphs = {}
+        self.launches_per_step = sum(1 + 3 * layers for _ in n_values)
+
+    # the four phases of one pass size
+    def _route(self, st):
+        api.route_topm(st["logits"], self.wl.m, ids=st["ids"], gates=st["gates"])
+
+    def _slot(self, st, n):
+        for l in range(self.L):
+            api.expert_op_perslot(self.layer, self.weights[l], st["x"], st["ids"][l * n:(l + 1) * n],
+                                  st["gates"][l * n:(l + 1) * n], y=st["y_slot"][l], accumulate=True, ws=self.ws)
+
+    def _group(self, st, n):
+        for l in range(self.L):
+            api.group_slots(st["ids"][l * n:(l + 1) * n], self.wl.N, out=st["groups"][l], ws=self.ws)
+
+    def _dedup(self, st, n):
+        for l in range(self.L):
+            api.expert_op_dedup(self.layer, self.weights[l], st["x"], st["gates"][l * n:(l + 1) * n],
+                                st["groups"][l], y=st["y_dedup"][l], accumulate=True, ws=self.ws)
+
+    def capture(self):
+        phases = ("route", "slot", "group", "dedup")
+        for n in self.n_values:
+            st = self.per_n[n]
+            self.stage(n, 0)
+            fns = {"route": lambda st=st: self._route(st), "slot": lambda st=st, n=n: self._slot(st, n),
+                   "group": lambda st=st, n=n: self._group(st, n), "dedup": lambda st=st, n=n: self._dedup(st, n)}
+            for ph in phases:      # eager run first: lazy initialisation outside capture
+                fns[ph]()
+            torch.cuda.synchronize(self.dev)
+            if self.use_graph:
+                for ph in phases:
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g):
+                        fns[ph]()
+                    self.graphs[(n, ph)] = g
+            else:
+                for ph in phases:
+                    self.graphs[(n, ph)] = fns[ph]
+        torch.cuda.synchronize(self.dev)
+        assert api.last_device_error(self.ws) == 0
+
+    def _run(self, n, ph):
+        g = self.graphs[(n, ph)]
+        g.replay() if self.use_graph else g()
+
+    def stage(self, n, w):
+        st = self.per_n[n]
+        st["logits"].copy_(st["logits_all"][w], non_blocking=True)
+        st["x"].copy_(st["x_all"][w], non_blocking=True)
+        st["y_slot"].zero_()
+        st["y_dedup"].zero_()
+
+    def step(self, w, events=None):
+        for n in self.n_values:
+            self.stage(n, w)
+            if events is not None:
+                events[(n, "start")].record()
+            for ph in ("route", "slot", "group", "dedup"):
+                self._run(n, ph)
+                if events is not None:
+                    events[(n, ph)].record()
+
+    def check_outputs(self):
+        """Cheap self-check after timing: ids equal the trace sets, forms agree."""
+        worst = 0.0
+        for n in self.n_values:
+            st = self.per_n[n]
+            ys, yd = st["y_slot"].double(), st["y_dedup"].double()
+            rms = ys.pow(2).mean().sqrt().clamp_min(1e-30)
+            worst = max(worst, float((ys - yd).abs().max() / rms))
+        return worst
+
+
+def run_ours(args, world, rank, local):
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    mbuild.build()
+    api.lib()
+    wl = BY_NAME[args.workload]
+    if wl.layers < 2 and args.layers is None:
+        raise SystemExit("bench.py times the multi-layer stack; single layers are parity-test cases")
+    layers = args.layers or wl.layers
+    n_max = args.n_max or max(wl.n_values)
+    n_values = [n for n in wl.n_values if n <= n_max]
+    windows = args.warmup + args.steps
+    b = StackBench(wl, layers, n_values, windows, device, use_graph=not args.no_graph)
+    b.capture()
+
+    for w in range(args.warmup):
+        b.step(w)
+    torch.cuda.synchronize(device)
+
+    phases = ("route", "slot", "group", "dedup")
+    events = [{(n, k): torch.cuda.Event(enable_timing=True) for n in n_values for k in ("start",) + phases}
+              for _ in range(args.steps)]
+    acc = {(n, ph): 0.0 for n in n_values for ph in phases}
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    with ClockSampler(local) as clk:
+        t_start.record()
+        for k in range(args.steps):
+            b.step(args.warmup + k, events[k])
+        t_end.record()
+        torch.cuda.synchronize(device)
+    barrier(world)
+    for k in range(args.steps):
+        for n in n_values:
+            prev = events[k][(n, "start")]
+            for ph in phases:
+                acc[(n, ph)] += prev.elapsed_time(events[k][(n, ph)]) * 1e-3
+                prev = events[k][(n, ph)]
+    total_s = t_start.elapsed_time(t_end) * 1e-3
+    total_s = reduce_max(total_s, world, device)
+    self_check = b.check_outputs()
+    err = api.last_device_error(b.ws)
+
+    # bytes requested in the timed steps
+    steps_w = range(args.warmup, args.warmup + args.steps)
+    bytes_slot = {n: sum(b.per_n[n]["bytes_slot"][w] for w in steps_w) for n in n_values}
+    bytes_dedup = {n: sum(b.per_n[n]["bytes_dedup"][w] for w in steps_w) for n in n_values}
+    total_bytes = sum(bytes_slot.values()) + sum(bytes_dedup.values())
+    value = world * total_bytes / total_s / 1e12
+    t_slot = [acc[(n, "slot")] for n in n_values]
+    t_dedup = [acc[(n, "group")] + acc[(n, "dedup")] for n in n_values]
+    rep = api.bandwidth_report(n_values[0], [bytes_slot[n] for n in n_values],
+                               [bytes_dedup[n] for n in n_values], t_slot, t_dedup)
+    K = args.steps
+    per_n = []
+    for i, n in enumerate(n_values):
+        per_n.append(dict(
+            n=n,
+            us_slot=round(t_slot[i] / K * 1e6, 2), us_dedup=round(t_dedup[i] / K * 1e6, 2),
+            us_dedup_group=round(acc[(n, "group")] / K * 1e6, 2), us_route=round(acc[(n, "route")] / K * 1e6, 2),
+            tbps_slot=round(rep["beta_slot"][i] / 1e12, 3), tbps_dedup=round(rep["beta_dedup"][i] / 1e12, 3),
+            tbps_dedup_kernel=round(bytes_dedup[n] / acc[(n, "dedup")] / 1e12, 3),
+            ubar=round(float(rep["ubar"][i]), 4), r=round(float(rep["r"][i]), 4),
+            saving_us=round(float(rep["saving"][i]) / K * 1e6, 2)))
+    # best draft length: V(k) = expert time of a pass of k+1 tokens (all layers)
+    kstar = {}
+    if n_values[0] == 1:
+        Vs = [t / K for t in t_slot]
+        Vd = [t_slot[0] / K] + [t / K for t in t_dedup[1:]]
+        cross = rep["crossover"]
+        Vw = [Vs[i] if (cross is None or n_values[i] < cross) else Vd[i] for i in range(len(n_values))]
+        for a in A_GRID:
+            kstar[str(a)] = dict(slot=api.best_draft_length(Vs, a), dedup=api.best_draft_length(Vd, a),
+                                 switched=api.best_draft_length(Vw, a))
+
+    # roofline of the expert kernel (both forms; one launch = one layer's expert op)
+    expert_s = sum(acc[(n, "slot")] + acc[(n, "dedup")] for n in n_values)
+    launches = 2 * layers * len(n_values) * K
+    peaks, peak_kind = measured_peaks()
+    achieved = total_bytes / expert_s / 1e9
+    traffic = kernel_traffic("expert_tc_kernel")
+    roofline = dict(kernel="expert_tc_kernel", bound="hbm", achieved=round(achieved, 1),
+                    peak=peaks["hbm_gbs"], unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4),
+                    peak_source=f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+                    bytes_per_launch=round(total_bytes / launches), mean_launch_us=round(expert_s / launches * 1e6, 2),
+                    traffic=(traffic or {}).get("dram_bytes_per_launch"),
+                    traffic_note=(traffic or {}).get("note"))
+
+    line = dict(metric=METRIC, value=round(value, 4), unit=UNIT, n_gpus=world, steps=K, warmup=args.warmup,
+                ms_per_step=round(total_s / K * 1e3, 3), higher_is_better=True, scaling="weak",
+                vs_baseline=None, dtype="bf16", data="synthetic",
+                config=dict(workload=wl.name, layers=layers, d=wl.d, f=wl.f, N=wl.N, m=wl.m,
+                            n_values=f"{n_values[0]}..{n_values[-1]}", rho=wl.rhos[0], parallelism="replicas",
+                            windows_per_step=1, graphs=not args.no_graph,
+                            l2="inputs larger than L2: 57.98 GB of weights streamed layer after layer"
+                            if layers == 48 else f"{layers} layers, no flush"),
+                roofline=roofline, gpu_launches=b.launches_per_step * K,
+                clocks=clk.summary(), per_n=per_n, crossover=rep["crossover"], kstar=kstar,
+                self_check=dict(max_slot_vs_dedup_rel=round(self_check, 6), device_error=err),
+                setup_s=dict(weights=round(b.t_weights, 1)))
+
+    if not args.no_e2e:
+        line["e2e"] = e2e_run(b, args, world, device, total_bytes_per_step=total_bytes / K)
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(b)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def e2e_run(b: StackBench, args, world, device, total_bytes_per_step):
+    """The same steps with inputs copied from pinned host memory and outputs copied back."""
+    host = {}
+    h2d = d2h = 0
+    for n in b.n_values:
+        st = b.per_n[n]
+        host[n] = dict(logits=st["logits_all"].cpu().pin_memory(), x=st["x_all"].cpu().pin_memory(),
+                       y_slot=torch.empty(st["y_slot"].shape, dtype=torch.float32).pin_memory(),
+                       y_dedup=torch.empty(st["y_dedup"].shape, dtype=torch.float32).pin_memory())
+        h2d += st["logits"].numel() * 4 + st["x"].numel() * 2
+        d2h += 2 * st["y_slot"].numel() * 4
+
+    def step(w):
+        for n in b.n_values:
+            st, hs = b.per_n[n], host[n]
+            st["logits"].copy_(hs["logits"][w], non_blocking=True)
+            st["x"].copy_(hs["x"][w], non_blocking=True)
+            st["y_slot"].zero_()
+            st["y_dedup"].zero_()
+            for ph in ("route", "slot", "group", "dedup"):
+                b._run(n, ph)
+            hs["y_slot"].copy_(st["y_slot"], non_blocking=True)
+            hs["y_dedup"].copy_(st["y_dedup"], non_blocking=True)
+
+    for w in range(args.warmup):
+        step(w)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for k in range(args.steps):
+        step(args.warmup + k)
+    e.record()
+    torch.cuda.synchronize(device)
+    t = reduce_max(s.elapsed_time(e) * 1e-3, world, device)
+    return dict(value=round(world * total_bytes_per_step * args.steps / t / 1e12, 4), unit=UNIT,
+                h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h, ms_per_step=round(t / args.steps * 1e3, 3))
+
+
+# --------------------------------------------------------------------- oracle timing
+
+def _oracle_sample(oracle_mod, wl, host_w, sets_l, x_host, n_list, budget_s):
+    """Time the oracle (both forms) on passes of layer 0; returns (bytes, seconds, passes)."""
+    w_bytes = wl.expert_bytes
+    done_bytes, done_s, passes = 0, 0.0, []
+    for n in n_list:
+        ids_set = sets_l[:n]
+        # the oracle routes from logits whose top-m is the set; use its grouping and bytes
+        z = np.full((n, wl.N), -10.0, np.float32)
+        for t in range(n):
+            z[t, ids_set[t]] = np.linspace(1.0, 0.5, wl.m, dtype=np.float32)
+        xh = x_host[:n]
+        t0 = time.perf_counter()
+        ids, gates = oracle_mod.route_topm(z, wl.m)
+        oracle_mod.expert_op_perslot(*host_w, xh, ids, gates)
+        grp = oracle_mod.group_slots(ids, wl.N)
+        oracle_mod.expert_op_dedup(*host_w, xh, gates, wl.m, grp)
+        done_s += time.perf_counter() - t0
+        done_bytes += n * wl.m * w_bytes + grp[0] * w_bytes
+        passes.append(n)
+        if done_s > budget_s:
+            break
+    return done_bytes, done_s, passes
+
+
+def cpu_baseline(b: StackBench):
+    import oracle
+    oracle.build()
+    wl = b.wl
+    host_w = tuple(synth.host_array(t) for t in b.weights[0])
+    x_host = synth.host_array(b.per_n[max(b.n_values)]["x_all"][0])
+    nb, s, passes = _oracle_sample(oracle, wl, host_w, b.sets[0], x_host, [1, 4, 16], budget_s=20.0)
+    return dict(value=round(nb / s / 1e12, 8), unit=UNIT, cores=1, kind="oracle",
+                sample=f"layer 0 of the stack, one pass at n in {passes}, per-slot and dedup forms "
+                       f"(routing, grouping, both expert ops, combine); {nb / 1e9:.2f} GB requested in {s:.1f} s")
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: each step is one pass of one layer (both forms)."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    wl = BY_NAME[args.workload]
+    n_max = args.n_max or max(wl.n_values)
+    wg, wu, wd = synth.expert_weights(wl.N, wl.f, wl.d, torch.bfloat16, synth.seed_for(wl.index, layer=0))
+    host_w = tuple(synth.host_array(t) for t in (wg, wu, wd))
+    T = (args.warmup + args.steps) * n_max
+    sets, _ = synth.routing_traces(1, T, wl.N, wl.m, wl.rhos[0], seed=synth.seed_for(wl.index, stream=2))
+    x_host = synth.host_array(synth.activations(n_max, wl.d, torch.bfloat16, seed=synth.seed_for(wl.index, stream=1)))
+    n_step = [1 + (k * 5) % n_max for k in range(args.warmup + args.steps)]   # cycle over pass sizes
+    for k in range(args.warmup):
+        _oracle_sample(oracle, wl, host_w, sets[0][k * n_max:], x_host, [n_step[k]], budget_s=1e9)
+    nb_tot, s_tot = 0, 0.0
+    for k in range(args.warmup, args.warmup + args.steps):
+        nb, s, _ = _oracle_sample(oracle, wl, host_w, sets[0][k * n_max:], x_host, [n_step[k]], budget_s=1e9)
+        nb_tot += nb
+        s_tot += s
+    value = nb_tot / s_tot / 1e12
+    sample = (f"one layer of {wl.name}, one pass per step at n in {n_step[args.warmup:]}, "
+              f"per-slot and dedup forms, single-threaded fp64 C oracle")
+    line = dict(metric=METRIC, value=round(value, 8), unit=UNIT, n_gpus=world, steps=args.steps,
+                warmup=args.warmup, ms_per_step=round(s_tot / args.steps * 1e3, 1), higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="f64", data="synthetic", impl="reference",
+                config=dict(workload=wl.name, layers=1, d=wl.d, f=wl.f, N=wl.N, m=wl.m, rho=wl.rhos[0]),
+                cpu_baseline=dict(value=round(value, 8), unit=UNIT, cores=1, kind="oracle", sample=sample),
+                e2e=dict(value=round(value, 8), unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

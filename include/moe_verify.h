@@ -61,12 +61,19 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
  * Weight layouts (row-major, one contiguous block per expert, nn.Linear convention):
  *   w_gate, w_up  [N, f, d];   w_down  [N, d, f].
  * Supported: 1 <= m <= N <= 1024, d and f multiples of 64, d <= 8192, f <= 65536;
- * (w_dtype, x_dtype) = (MOE_BF16, MOE_BF16) or (MOE_F32, MOE_F32).
+ * (w_dtype, x_dtype) = (MOE_BF16, MOE_BF16) or (MOE_F32, MOE_F32).  The tensor-core
+ * kernel takes bf16 layers with d a multiple of 128 and d <= 4096; other bf16 shapes
+ * run on the CUDA-core kernel.
  */
 typedef struct {
     int32_t d, f, N, m;
     int32_t w_dtype, x_dtype;
+    int32_t flags;   /* 0, or MOE_FLAG_SIMT */
 } moe_layer_t;
+
+/* flags: run the expert operation on the CUDA-core kernel even for bf16 layers (the
+ * tensor-core kernel is the default for bf16; fp32 layers always use the CUDA cores). */
+#define MOE_FLAG_SIMT 1
 
 /* Largest pass size (tokens per verification pass) the expert operation accepts. */
 #define MOE_MAX_PASS_TOKENS 16

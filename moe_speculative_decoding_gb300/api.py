@@ -1,0 +1,261 @@
+"""Python binding of libmoeverify.so: argument marshalling only.
+
+Every step of the verify-pass expert operation runs in the library's CUDA kernels; this
+module checks tensor devices, dtypes and shapes, passes raw pointers and the current
+torch stream, and turns status codes into exceptions.  There is no fallback: if the
+library is missing, every call raises MoeError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+MOE_F32, MOE_BF16 = 0, 1
+MOE_FLAG_SIMT = 1
+MAX_PASS_TOKENS = 16
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
+          4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_BAD_ID", 6: "MOE_ERR_DEVICE_TIMEOUT"}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {STATUS.get(code, code)}")
+
+
+class Layer(ctypes.Structure):
+    _fields_ = [("d", ctypes.c_int32), ("f", ctypes.c_int32), ("N", ctypes.c_int32),
+                ("m", ctypes.c_int32), ("w_dtype", ctypes.c_int32), ("x_dtype", ctypes.c_int32),
+                ("flags", ctypes.c_int32)]
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.w_dtype == MOE_BF16 else torch.float32
+
+
+class _PassBytes(ctypes.Structure):
+    _fields_ = [("expert_bytes", ctypes.c_uint64), ("slot_bytes", ctypes.c_uint64),
+                ("dedup_bytes", ctypes.c_uint64), ("act_bytes", ctypes.c_uint64),
+                ("n", ctypes.c_int32), ("m", ctypes.c_int32), ("U", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("ubar", ctypes.c_double)]
+
+
+EXPORTED = ("moe_abi_version", "moe_status_str", "moe_workspace_bytes", "moe_workspace_init",
+            "moe_route_topm", "moe_group_slots", "moe_expert_op_perslot", "moe_expert_op_dedup",
+            "moe_pass_bytes", "moe_bandwidth_report", "moe_expected_union",
+            "moe_best_draft_length", "moe_last_device_error")
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded library.  Raises MoeError if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise MoeError(-1, f"libmoeverify.so not built at {path} "
+                           "(run python -m moe_speculative_decoding_gb300.build)")
+    L = ctypes.CDLL(path)
+    P, I32, SZ, D = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_double
+    LP = ctypes.POINTER(Layer)
+    sig = {
+        "moe_abi_version": ([], I32),
+        "moe_status_str": ([I32], ctypes.c_char_p),
+        "moe_workspace_bytes": ([LP, I32], SZ),
+        "moe_workspace_init": ([P, SZ, P], I32),
+        "moe_route_topm": ([P, I32, I32, I32, I32, P, P, P], I32),
+        "moe_group_slots": ([P, I32, I32, I32, P, P, P, P, P, P], I32),
+        "moe_expert_op_perslot": ([LP, P, P, P, P, P, P, I32, I32, P, P, SZ, P], I32),
+        "moe_expert_op_dedup": ([LP, P, P, P, P, P, I32, P, P, P, P, I32, P, P, SZ, P], I32),
+        "moe_pass_bytes": ([LP, P, I32, ctypes.POINTER(_PassBytes)], I32),
+        "moe_bandwidth_report": ([I32, I32, P, P, P, P, P, P, P, P, P, P], I32),
+        "moe_expected_union": ([I32, I32, I32], D),
+        "moe_best_draft_length": ([P, I32, D], I32),
+        "moe_last_device_error": ([P, P, P], I32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = L
+    return L
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise MoeError(code, what)
+
+
+def _stream(device=None):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+# ---------------------------------------------------------------- layer + workspace
+
+def make_layer(d: int, f: int, N: int, m: int, dtype: str = "bf16", simt: bool = False) -> Layer:
+    code = MOE_BF16 if dtype == "bf16" else MOE_F32
+    return Layer(d, f, N, m, code, code, MOE_FLAG_SIMT if simt else 0)
+
+
+def workspace(layer: Layer, n_max: int = MAX_PASS_TOKENS, device=None) -> torch.Tensor:
+    nbytes = int(lib().moe_workspace_bytes(ctypes.byref(layer), n_max))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+    _check(lib().moe_workspace_init(ctypes.c_void_p(ws.data_ptr()), nbytes, _stream(ws.device)),
+           "moe_workspace_init")
+    return ws
+
+
+def last_device_error(ws: torch.Tensor) -> int:
+    code = ctypes.c_int32(0)
+    _check(lib().moe_last_device_error(ctypes.c_void_p(ws.data_ptr()), _stream(ws.device),
+                                       ctypes.byref(code)), "moe_last_device_error")
+    return int(code.value)
+
+
+# ---------------------------------------------------------------- the hot path
+
+def route_topm(logits: torch.Tensor, m: int, renorm: bool = True, ids=None, gates=None):
+    """Top-m routing of fp32 logits [n, N] -> (ids int32 [n, m], gates fp32 [n, m])."""
+    n, N = logits.shape
+    if ids is None:
+        ids = torch.empty((n, m), dtype=torch.int32, device=logits.device)
+    if gates is None:
+        gates = torch.empty((n, m), dtype=torch.float32, device=logits.device)
+    _check(lib().moe_route_topm(_dev(logits, "logits", torch.float32), n, N, m, int(bool(renorm)),
+                                _dev(ids, "ids", torch.int32, (n, m)),
+                                _dev(gates, "gates", torch.float32, (n, m)), _stream(logits.device)),
+           "moe_route_topm")
+    return ids, gates
+
+
+@dataclass
+class Grouping:
+    num_distinct: torch.Tensor   # int32 [1]
+    expert_list: torch.Tensor    # int32 [min(N, n*m)]
+    offsets: torch.Tensor        # int32 [min(N, n*m) + 1]
+    slot_order: torch.Tensor     # int32 [n*m]
+
+    @staticmethod
+    def empty(n: int, m: int, N: int, device) -> "Grouping":
+        cap = min(N, n * m)
+        z = lambda k: torch.zeros(k, dtype=torch.int32, device=device)
+        return Grouping(z(1), z(max(cap, 1)), z(cap + 1), z(n * m))
+
+
+def group_slots(ids: torch.Tensor, N: int, out: Grouping | None = None, ws=None) -> Grouping:
+    n, m = ids.shape
+    g = out or Grouping.empty(n, m, N, ids.device)
+    _check(lib().moe_group_slots(_dev(ids, "ids", torch.int32), n, m, N,
+                                 _dev(g.num_distinct, "num_distinct"), _dev(g.expert_list, "expert_list"),
+                                 _dev(g.offsets, "offsets"), _dev(g.slot_order, "slot_order"),
+                                 ctypes.c_void_p(ws.data_ptr()) if ws is not None else None,
+                                 _stream(ids.device)), "moe_group_slots")
+    return g
+
+
+def _weights(layer: Layer, weights):
+    wg, wu, wd = weights
+    dt = layer.torch_dtype
+    return (_dev(wg, "w_gate", dt, (layer.N, layer.f, layer.d)),
+            _dev(wu, "w_up", dt, (layer.N, layer.f, layer.d)),
+            _dev(wd, "w_down", dt, (layer.N, layer.d, layer.f)))
+
+
+def _y(layer, x, y):
+    n = x.shape[0]
+    if y is None:
+        y = torch.empty((n, layer.d), dtype=torch.float32, device=x.device)
+    return y, _dev(y, "y", torch.float32, (n, layer.d))
+
+
+def expert_op_perslot(layer: Layer, weights, x: torch.Tensor, ids: torch.Tensor, gates: torch.Tensor,
+                      y=None, accumulate: bool = False, ws=None):
+    n = x.shape[0]
+    ws = ws if ws is not None else workspace(layer, n, x.device)
+    y, yp = _y(layer, x, y)
+    _check(lib().moe_expert_op_perslot(ctypes.byref(layer), *_weights(layer, weights),
+                                       _dev(x, "x", layer.torch_dtype, (n, layer.d)),
+                                       _dev(ids, "ids", torch.int32, (n, layer.m)),
+                                       _dev(gates, "gates", torch.float32, (n, layer.m)), n,
+                                       int(bool(accumulate)), yp, ctypes.c_void_p(ws.data_ptr()),
+                                       ws.numel(), _stream(x.device)), "moe_expert_op_perslot")
+    return y
+
+
+def expert_op_dedup(layer: Layer, weights, x: torch.Tensor, gates: torch.Tensor, grouping: Grouping,
+                    y=None, accumulate: bool = False, ws=None):
+    n = x.shape[0]
+    ws = ws if ws is not None else workspace(layer, n, x.device)
+    y, yp = _y(layer, x, y)
+    _check(lib().moe_expert_op_dedup(ctypes.byref(layer), *_weights(layer, weights),
+                                     _dev(x, "x", layer.torch_dtype, (n, layer.d)),
+                                     _dev(gates, "gates", torch.float32, (n, layer.m)), n,
+                                     _dev(grouping.num_distinct, "num_distinct"),
+                                     _dev(grouping.expert_list, "expert_list"),
+                                     _dev(grouping.offsets, "offsets"),
+                                     _dev(grouping.slot_order, "slot_order"),
+                                     int(bool(accumulate)), yp, ctypes.c_void_p(ws.data_ptr()),
+                                     ws.numel(), _stream(x.device)), "moe_expert_op_dedup")
+    return y
+
+
+# ---------------------------------------------------------------- host-side report
+
+def pass_bytes(layer: Layer, ids_host) -> dict:
+    ids = np.ascontiguousarray(np.asarray(ids_host, dtype=np.int32))
+    n = ids.shape[0] if ids.ndim == 2 else ids.size // layer.m
+    out = _PassBytes()
+    _check(lib().moe_pass_bytes(ctypes.byref(layer), ctypes.c_void_p(ids.ctypes.data), n,
+                                ctypes.byref(out)), "moe_pass_bytes")
+    return dict(expert_bytes=out.expert_bytes, slot_bytes=out.slot_bytes, dedup_bytes=out.dedup_bytes,
+                act_bytes=out.act_bytes, n=out.n, m=out.m, U=out.U, ubar=out.ubar)
+
+
+def bandwidth_report(n_lo: int, slot_bytes, dedup_bytes, t_slot, t_dedup) -> dict:
+    arrs = [np.ascontiguousarray(np.asarray(a, dtype=np.float64)) for a in
+            (slot_bytes, dedup_bytes, t_slot, t_dedup)]
+    count = arrs[0].size
+    outs = [np.zeros(count, np.float64) for _ in range(5)]
+    cross = ctypes.c_int32(0)
+    _check(lib().moe_bandwidth_report(n_lo, count, *[ctypes.c_void_p(a.ctypes.data) for a in arrs],
+                                      *[ctypes.c_void_p(o.ctypes.data) for o in outs],
+                                      ctypes.byref(cross)), "moe_bandwidth_report")
+    res = dict(zip(("beta_slot", "beta_dedup", "ubar", "r", "saving"), outs))
+    res["crossover"] = None if cross.value < 0 else int(cross.value)
+    return res
+
+
+def expected_union(N: int, m: int, n: int) -> float:
+    return float(lib().moe_expected_union(N, m, n))
+
+
+def best_draft_length(V, a: float) -> int:
+    V = np.ascontiguousarray(np.asarray(V, dtype=np.float64))
+    k = int(lib().moe_best_draft_length(ctypes.c_void_p(V.ctypes.data), V.size - 1, float(a)))
+    if k < 0:
+        raise MoeError(1, "moe_best_draft_length")
+    return k

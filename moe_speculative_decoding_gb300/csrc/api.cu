@@ -1,0 +1,275 @@
+// api.cu -- the C ABI of libmoeverify.so (declared in include/moe_verify.h).
+//
+// Host-side validation, dispatch to the kernels, and the host-only report math of
+// "Speculative Decoding for Mixture-of-Experts Models" (Lan): requested bytes (§1
+// "Bytes"), effective bandwidth, u_bar and r (§2), the saving and the crossover (§3.1,
+// §2 "Testing the inputs"), E[U] under uniform routing (§1) and the best draft length
+// (§1 "Speculative decoding").
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+#include "common.cuh"
+#include "expert_args.cuh"
+
+namespace moe {
+cudaError_t launch_route_topm(const float *logits, int n, int N, int m, int renorm, int32_t *ids, float *gates,
+                              cudaStream_t s, bool pdl);
+cudaError_t launch_group_slots(const int32_t *ids, int S, int N, int32_t *num_distinct, int32_t *expert_list,
+                               int32_t *offsets, int32_t *order, int32_t *err, cudaStream_t s, bool pdl);
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+constexpr bool kUsePdl = true;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status_t check_layer(const moe_layer_t *L) {
+    if (L == nullptr) return MOE_ERR_ARG;
+    if (L->d <= 0 || L->f <= 0 || L->N <= 0 || L->m <= 0) return MOE_ERR_ARG;
+    if (L->m > L->N || L->N > 1024) return MOE_ERR_UNSUPPORTED;
+    if (L->d % 64 != 0 || L->f % 64 != 0 || L->d > 8192 || L->f > 65536) return MOE_ERR_UNSUPPORTED;
+    const bool bf = L->w_dtype == MOE_BF16 && L->x_dtype == MOE_BF16;
+    const bool fp = L->w_dtype == MOE_F32 && L->x_dtype == MOE_F32;
+    if (!bf && !fp) return MOE_ERR_UNSUPPORTED;
+    if ((L->flags & ~MOE_FLAG_SIMT) != 0) return MOE_ERR_ARG;
+    return MOE_OK;
+}
+
+moe_status_t check_expert_common(const moe_layer_t *L, const void *wg, const void *wu, const void *wd,
+                                 const void *x, const float *gates, int32_t n, const float *y, const void *ws,
+                                 size_t ws_bytes) {
+    moe_status_t st = check_layer(L);
+    if (st != MOE_OK) return st;
+    if (n < 1) return MOE_ERR_ARG;
+    if (n > MOE_MAX_PASS_TOKENS) return MOE_ERR_UNSUPPORTED;
+    const void *ptrs[] = {wg, wu, wd, x, gates, y};
+    for (const void *p : ptrs)
+        if (p == nullptr || !aligned16(p)) return MOE_ERR_ARG;
+    if (ws == nullptr || ws_bytes < kWorkspaceBytes) return MOE_ERR_WORKSPACE;
+    if (!aligned16(ws)) return MOE_ERR_ARG;
+    return MOE_OK;
+}
+
+ExpertArgs make_args(const moe_layer_t *L, const void *wg, const void *wu, const void *wd, const void *x,
+                     const float *gates, int32_t n, float *y, void *ws, int mode) {
+    ExpertArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.w_gate = wg;
+    a.w_up = wu;
+    a.w_down = wd;
+    a.x = x;
+    a.gates = gates;
+    a.y = y;
+    a.err = &static_cast<DeviceWorkspace *>(ws)->error;
+    a.d = L->d;
+    a.f = L->f;
+    a.N = L->N;
+    a.m = L->m;
+    a.n = n;
+    a.mode = mode;
+    a.w_dtype = L->w_dtype;
+    a.x_dtype = L->x_dtype;
+    return a;
+}
+
+moe_status_t run_expert(const moe_layer_t *L, const ExpertArgs &a, int max_groups, int32_t accumulate,
+                        cudaStream_t s) {
+    if (!accumulate) {
+        cudaError_t e = cudaMemsetAsync(a.y, 0, sizeof(float) * static_cast<size_t>(a.n) * a.d, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    const bool use_tc = L->w_dtype == MOE_BF16 && !(L->flags & MOE_FLAG_SIMT) && expert_tc_supports(L->d, L->f);
+    cudaError_t e = use_tc ? launch_expert_tc(a, max_groups, s, kUsePdl) : launch_expert_simt(a, max_groups, s, kUsePdl);
+    if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char *moe_status_str(moe_status_t status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_ARG: return "invalid argument (null pointer, bad size or misaligned buffer)";
+        case MOE_ERR_UNSUPPORTED: return "sizes or dtypes outside the supported range";
+        case MOE_ERR_CUDA: return "a CUDA call or kernel launch failed";
+        case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+        case MOE_ERR_BAD_ID: return "an expert id outside [0, N) was skipped";
+        case MOE_ERR_DEVICE_TIMEOUT: return "a device pipeline wait timed out";
+    }
+    return "unknown status";
+}
+
+size_t moe_workspace_bytes(const moe_layer_t *layer, int32_t n_max) {
+    (void)layer;
+    (void)n_max;
+    return kWorkspaceBytes;
+}
+
+moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t s) {
+    if (ws == nullptr || ws_bytes < kWorkspaceBytes) return MOE_ERR_WORKSPACE;
+    if (!aligned16(ws)) return MOE_ERR_ARG;
+    return cuda_status(cudaMemsetAsync(ws, 0, kWorkspaceBytes, reinterpret_cast<cudaStream_t>(s)));
+}
+
+moe_status_t moe_route_topm(const float *logits, int32_t n, int32_t N, int32_t m, int32_t renorm, int32_t *ids,
+                            float *gates, moe_stream_t s) {
+    if (n < 0 || N < 1 || m < 1) return MOE_ERR_ARG;
+    if (m > N || N > 1024 || m > 32) return MOE_ERR_UNSUPPORTED;
+    if (n == 0) return MOE_OK;
+    if (logits == nullptr || ids == nullptr || gates == nullptr) return MOE_ERR_ARG;
+    if (!aligned16(logits) || !aligned16(ids) || !aligned16(gates)) return MOE_ERR_ARG;
+    cudaError_t e = launch_route_topm(logits, n, N, m, renorm, ids, gates, reinterpret_cast<cudaStream_t>(s), kUsePdl);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return cuda_status(e);
+}
+
+moe_status_t moe_group_slots(const int32_t *ids, int32_t n, int32_t m, int32_t N, int32_t *num_distinct,
+                             int32_t *expert_list, int32_t *expert_offsets, int32_t *slot_order, void *ws,
+                             moe_stream_t s) {
+    if (n < 1 || m < 1 || N < 1) return MOE_ERR_ARG;
+    if (static_cast<int64_t>(n) * m > 4096 || N > 1024) return MOE_ERR_UNSUPPORTED;
+    const void *ptrs[] = {ids, num_distinct, expert_list, expert_offsets, slot_order};
+    for (const void *p : ptrs)
+        if (p == nullptr || !aligned16(p)) return MOE_ERR_ARG;
+    if (ws != nullptr && !aligned16(ws)) return MOE_ERR_ARG;
+    int32_t *err = ws ? &static_cast<DeviceWorkspace *>(ws)->error : nullptr;
+    cudaError_t e = launch_group_slots(ids, n * m, N, num_distinct, expert_list, expert_offsets, slot_order, err,
+                                       reinterpret_cast<cudaStream_t>(s), kUsePdl);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return cuda_status(e);
+}
+
+moe_status_t moe_expert_op_perslot(const moe_layer_t *layer, const void *w_gate, const void *w_up,
+                                   const void *w_down, const void *x, const int32_t *ids, const float *gates,
+                                   int32_t n, int32_t accumulate, float *y, void *ws, size_t ws_bytes,
+                                   moe_stream_t s) {
+    moe_status_t st = check_expert_common(layer, w_gate, w_up, w_down, x, gates, n, y, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (ids == nullptr || !aligned16(ids)) return MOE_ERR_ARG;
+    ExpertArgs a = make_args(layer, w_gate, w_up, w_down, x, gates, n, y, ws, kModePerSlot);
+    a.ids = ids;
+    return run_expert(layer, a, n * layer->m, accumulate, reinterpret_cast<cudaStream_t>(s));
+}
+
+moe_status_t moe_expert_op_dedup(const moe_layer_t *layer, const void *w_gate, const void *w_up,
+                                 const void *w_down, const void *x, const float *gates, int32_t n,
+                                 const int32_t *num_distinct, const int32_t *expert_list,
+                                 const int32_t *expert_offsets, const int32_t *slot_order, int32_t accumulate,
+                                 float *y, void *ws, size_t ws_bytes, moe_stream_t s) {
+    moe_status_t st = check_expert_common(layer, w_gate, w_up, w_down, x, gates, n, y, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    const void *ptrs[] = {num_distinct, expert_list, expert_offsets, slot_order};
+    for (const void *p : ptrs)
+        if (p == nullptr || !aligned16(p)) return MOE_ERR_ARG;
+    ExpertArgs a = make_args(layer, w_gate, w_up, w_down, x, gates, n, y, ws, kModeDedup);
+    a.num_distinct = num_distinct;
+    a.expert_list = expert_list;
+    a.offsets = expert_offsets;
+    a.slot_order = slot_order;
+    const int cap = n * layer->m < layer->N ? n * layer->m : layer->N;
+    return run_expert(layer, a, cap, accumulate, reinterpret_cast<cudaStream_t>(s));
+}
+
+moe_status_t moe_pass_bytes(const moe_layer_t *layer, const int32_t *ids_host, int32_t n, moe_pass_bytes_t *out) {
+    moe_status_t st = check_layer(layer);
+    if (st != MOE_OK) return st;
+    if (ids_host == nullptr || out == nullptr || n < 0) return MOE_ERR_ARG;
+    std::vector<uint8_t> seen(static_cast<size_t>(layer->N), 0);
+    int32_t U = 0;
+    const int64_t S = static_cast<int64_t>(n) * layer->m;
+    for (int64_t s = 0; s < S; ++s) {
+        const int32_t e = ids_host[s];
+        if (e < 0 || e >= layer->N) return MOE_ERR_BAD_ID;
+        if (!seen[e]) {
+            seen[e] = 1;
+            ++U;
+        }
+    }
+    const uint64_t wsz = layer->w_dtype == MOE_BF16 ? 2u : 4u;
+    const uint64_t xsz = layer->x_dtype == MOE_BF16 ? 2u : 4u;
+    out->expert_bytes = 3ull * static_cast<uint64_t>(layer->d) * static_cast<uint64_t>(layer->f) * wsz;
+    out->slot_bytes = static_cast<uint64_t>(S) * out->expert_bytes;
+    out->dedup_bytes = static_cast<uint64_t>(U) * out->expert_bytes;
+    out->act_bytes = static_cast<uint64_t>(n) * layer->d * xsz + static_cast<uint64_t>(n) * layer->d * 4ull;
+    out->n = n;
+    out->m = layer->m;
+    out->U = U;
+    out->reserved = 0;
+    out->ubar = S > 0 ? static_cast<double>(U) / static_cast<double>(S) : 0.0;
+    return MOE_OK;
+}
+
+moe_status_t moe_bandwidth_report(int32_t n_lo, int32_t count, const double *slot_bytes, const double *dedup_bytes,
+                                  const double *t_slot, const double *t_dedup, double *beta_slot,
+                                  double *beta_dedup, double *ubar, double *r, double *saving,
+                                  int32_t *crossover) {
+    if (count < 1 || !slot_bytes || !dedup_bytes || !t_slot || !t_dedup || !beta_slot || !beta_dedup || !ubar ||
+        !r || !saving || !crossover)
+        return MOE_ERR_ARG;
+    for (int32_t i = 0; i < count; ++i) {
+        if (!(t_slot[i] > 0.0) || !(t_dedup[i] > 0.0) || !(slot_bytes[i] > 0.0) || !(dedup_bytes[i] >= 0.0))
+            return MOE_ERR_ARG;
+    }
+    for (int32_t i = 0; i < count; ++i) {
+        beta_slot[i] = slot_bytes[i] / t_slot[i];
+        beta_dedup[i] = dedup_bytes[i] / t_dedup[i];
+        ubar[i] = dedup_bytes[i] / slot_bytes[i];
+        r[i] = beta_dedup[i] / beta_slot[i];
+        saving[i] = t_slot[i] - t_dedup[i];
+    }
+    // the smallest n from which the saving stays positive
+    int32_t cross = -1;
+    for (int32_t i = count - 1; i >= 0; --i) {
+        if (saving[i] > 0.0) cross = n_lo + i;
+        else break;
+    }
+    *crossover = cross;
+    return MOE_OK;
+}
+
+double moe_expected_union(int32_t N, int32_t m, int32_t n) {
+    if (N < 1 || m < 0 || m > N || n < 0) return NAN;
+    const double q = 1.0 - static_cast<double>(m) / static_cast<double>(N);
+    return static_cast<double>(N) * (1.0 - std::pow(q, static_cast<double>(n)));
+}
+
+int32_t moe_best_draft_length(const double *V, int32_t kmax, double a) {
+    if (V == nullptr || kmax < 0 || !(a >= 0.0) || !(a < 1.0)) return -1;
+    int32_t best = -1;
+    double best_T = 0.0, G = 0.0, p = 1.0;
+    for (int32_t k = 0; k <= kmax; ++k) {
+        if (!(V[k] > 0.0)) return -1;
+        G += p;   // G_a(k) = 1 + a + ... + a^k
+        p *= a;
+        const double T = G / V[k];
+        if (best < 0 || T > best_T) {
+            best = k;
+            best_T = T;
+        }
+    }
+    return best;
+}
+
+moe_status_t moe_last_device_error(void *ws, moe_stream_t s, int32_t *code) {
+    if (ws == nullptr || code == nullptr) return MOE_ERR_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    int32_t v = 0;
+    if (cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemset(ws, 0, sizeof v) != cudaSuccess) return MOE_ERR_CUDA;
+    *code = v;
+    return MOE_OK;
+}
+
+}  // extern "C"

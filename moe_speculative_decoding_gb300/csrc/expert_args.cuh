@@ -1,0 +1,41 @@
+// expert_args.cuh -- arguments shared by the expert-operation kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kMaxPassTokens = MOE_MAX_PASS_TOKENS;   // tokens per pass (MMA N = 16)
+constexpr int kFTile = 64;                             // rows of f per work item
+
+enum : int { kModePerSlot = 0, kModeDedup = 1 };
+
+// One call of the expert operation.  Per-slot form: group g is slot g (expert ids[g],
+// token g / m).  Deduplicating form: group g is expert_list[g] with the slots
+// slot_order[offsets[g] .. offsets[g+1]); the number of groups is num_distinct[0].
+struct ExpertArgs {
+    const void *w_gate;
+    const void *w_up;
+    const void *w_down;
+    const void *x;
+    const int32_t *ids;
+    const float *gates;
+    const int32_t *num_distinct;
+    const int32_t *expert_list;
+    const int32_t *offsets;
+    const int32_t *slot_order;
+    float *y;
+    int32_t *err;
+    int d, f, N, m, n, mode, w_dtype, x_dtype;
+};
+
+cudaError_t launch_expert_simt(const ExpertArgs &a, int groups, cudaStream_t s, bool pdl);
+
+// Tensor-core kernel (bf16).  Returns cudaErrorNotSupported when the shape is outside
+// what it handles (the caller then reports MOE_ERR_UNSUPPORTED).
+cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, cudaStream_t s, bool pdl);
+bool expert_tc_supports(int d, int f);
+
+}  // namespace moe

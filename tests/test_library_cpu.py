@@ -1,0 +1,115 @@
+"""The C-ABI library on the CPU: it builds, loads, exports every declared symbol, and its
+host-only calls (bytes, report math) agree with the oracle.  No kernel is launched."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT, load_golden
+from moe_speculative_decoding_gb300 import api, synth
+from moe_speculative_decoding_gb300 import build as mbuild
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mbuild.build()
+    return api.lib()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "moe_verify.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert len(declared) >= 13
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(declared) == set(api.EXPORTED)
+    assert lib.moe_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert len(lib.moe_status_str(code)) > 0
+    assert lib.moe_status_str(99) == b"unknown status"
+
+
+def test_argument_validation_before_any_launch(lib):
+    """Invalid arguments are rejected on the host, before anything touches the GPU."""
+    st = lib.moe_route_topm(None, 4, 8, 2, 1, None, None, None)
+    assert st == 1  # MOE_ERR_ARG
+    assert lib.moe_route_topm(None, 4, 8, 9, 1, None, None, None) == 2   # m > N
+    assert lib.moe_route_topm(None, 4, 2048, 2, 1, None, None, None) == 2  # N > 1024
+    assert lib.moe_group_slots(None, 64, 128, 8, None, None, None, None, None, None) == 2  # > 4096 slots
+    L = api.make_layer(2048, 768, 128, 8)
+    bad = api.make_layer(2048, 700, 128, 8)   # f not a multiple of 64
+    args = [None] * 6
+    assert lib.moe_expert_op_perslot(ctypes.byref(bad), *args, 4, 0, None, None, 0, None) == 2
+    # n above the pass limit
+    assert lib.moe_expert_op_perslot(ctypes.byref(L), *args, 17, 0, None, None, 0, None) == 2
+    # null pointers
+    assert lib.moe_expert_op_perslot(ctypes.byref(L), *args, 4, 0, None, None, 0, None) == 1
+    mixed = api.Layer(2048, 768, 128, 8, 1, 0, 0)   # bf16 weights with fp32 x
+    assert lib.moe_expert_op_dedup(ctypes.byref(mixed), *[None] * 5, 4, *[None] * 4, 0, None, None, 0,
+                                   None) == 2
+    assert lib.moe_workspace_init(None, 256, None) == 4
+    assert lib.moe_workspace_bytes(ctypes.byref(L), 16) >= 4
+
+
+def test_pass_bytes_matches_oracle(lib, oracle_mod):
+    rng = np.random.default_rng(40)
+    for (d, f, N, m, dt) in [(2048, 768, 128, 8, "bf16"), (2048, 1408, 64, 6, "bf16"),
+                             (4096, 14336, 8, 2, "bf16"), (256, 512, 8, 2, "f32")]:
+        L = api.make_layer(d, f, N, m, dt)
+        for n in (1, 3, 8, 16):
+            sets, _ = synth.routing_traces(1, n, N, m, float(rng.uniform(0, 1)), seed=int(rng.integers(1e9)))
+            ids = sets[0]
+            got = api.pass_bytes(L, ids)
+            code = 1 if dt == "bf16" else 0
+            ref = oracle_mod.pass_bytes(d, f, N, ids, code, code)
+            for k in ("expert_bytes", "slot_bytes", "dedup_bytes", "act_bytes", "U"):
+                assert got[k] == ref[k], k
+            assert got["ubar"] == ref["ubar"]
+    with pytest.raises(api.MoeError):
+        api.pass_bytes(api.make_layer(256, 512, 8, 2, "f32"), np.array([[0, 8]], np.int32))
+
+
+def test_bandwidth_report_matches_oracle(lib, oracle_mod):
+    rng = np.random.default_rng(41)
+    for _ in range(50):
+        k = int(rng.integers(1, 17))
+        sb = rng.uniform(1e7, 1e9, k)
+        db = sb * rng.uniform(0.2, 1.0, k)
+        ts = rng.uniform(1e-6, 1e-3, k)
+        td = ts * rng.uniform(0.5, 1.5, k)
+        got = api.bandwidth_report(1, sb, db, ts, td)
+        ref = oracle_mod.bandwidth_report(1, sb, db, ts, td)
+        for key in ("beta_slot", "beta_dedup", "ubar", "r", "saving"):
+            assert np.allclose(got[key], ref[key], rtol=1e-15, atol=0), key
+        assert got["crossover"] == ref["crossover"]
+    g = load_golden("table1_effective_bandwidth.json")
+    for row in g["rows"]:
+        _, _, bs, bd, r, u = row[:6]
+        rep = api.bandwidth_report(2, [1e9], [u * 1e9], [1e9 / bs], [u * 1e9 / bd])
+        assert abs(rep["r"][0] - r) <= g["rounding"]
+
+
+def test_expected_union_and_best_draft_length_match_oracle(lib, oracle_mod):
+    for (N, m) in [(128, 8), (64, 6), (8, 2), (4, 2)]:
+        for n in range(0, 17):
+            assert abs(api.expected_union(N, m, n) - oracle_mod.expected_union(N, m, n)) < 1e-12
+    g = load_golden("staircase_jump.json")
+    for a, kstar in g["cases"]:
+        assert api.best_draft_length(g["V"], a) == kstar
+    rng = np.random.default_rng(42)
+    for _ in range(200):
+        V = rng.uniform(0.2, 5.0, size=int(rng.integers(1, 10)))
+        a = float(rng.uniform(0, 0.99))
+        assert api.best_draft_length(V, a) == oracle_mod.best_draft_length(V, a)
+    with pytest.raises(api.MoeError):
+        api.best_draft_length([1.0, -1.0], 0.5)
