@@ -57,6 +57,7 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default=QWEN3_STACK.name, choices=sorted(BY_NAME))
     p.add_argument("--layers", type=int, default=None, help="override the stack depth (smaller test runs)")
+    p.add_argument("--n-min", type=int, default=None)
     p.add_argument("--n-max", type=int, default=None)
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -296,7 +297,7 @@ def run_ours(args, world, rank, local):
         raise SystemExit("bench.py times the multi-layer stack; single layers are parity-test cases")
     layers = args.layers or wl.layers
     n_max = args.n_max or max(wl.n_values)
-    n_values = [n for n in wl.n_values if n <= n_max]
+    n_values = [n for n in wl.n_values if (args.n_min or 1) <= n <= n_max]
     windows = args.warmup + args.steps
     b = StackBench(wl, layers, n_values, windows, device, use_graph=not args.no_graph)
     b.capture()

@@ -24,24 +24,33 @@ __device__ __forceinline__ void record_error(int32_t *err, int32_t code) {
     if (err != nullptr) atomicCAS(err, 0, code);
 }
 
-// Time limit of every spin-wait on an mbarrier (nanoseconds of %globaltimer).
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+// Time limit of every spin-wait on an mbarrier, in SM clock cycles (about 2 s at the
+// 2.07 GHz maximum clock; longer at lower clocks).
+constexpr long long kWaitLimitCycles = 4000000000ll;
 
 // ------------------------------------------------------------------ basics
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
 
 // Programmatic dependent launch: wait for the grids this one depends on (no-op when
 // the launch carried no programmatic dependency), and allow dependents to launch.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// One lane of the (fully active) warp returns true.  Issuing tensor-core and TMA
+// instructions from an elected lane inside warp-uniform code keeps their operands in
+// uniform registers; a lone divergent lane issuing them is several times slower.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(pred));
+    return pred != 0;
+}
 
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -70,16 +79,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity.  Gives up when *abort becomes
-// non-zero (another role gave up) or after kWaitLimitNs; on a time-out it raises the
+// non-zero (another role gave up) or after kWaitLimitCycles; on a time-out it raises the
 // abort flag and records MOE_ERR_DEVICE_TIMEOUT.  Returns true when the phase completed.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int32_t *abort,
                                           int32_t *err) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
+    const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (clock64() - t0 > kWaitLimitCycles) {
             *abort = 1;
             record_error(err, MOE_ERR_DEVICE_TIMEOUT);
             return false;
@@ -88,10 +97,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // Bounded wait that ignores the abort flag (used to drain copies in flight on abort).
-__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-    const uint64_t t0 = global_timer_ns();
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, long long limit_cycles) {
+    const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > limit_ns) return false;
+        if (clock64() - t0 > limit_cycles) return false;
     }
     return true;
 }

@@ -26,6 +26,12 @@
 //     form h = silu(g) * u for the tile (bf16, written to shared memory as the next
 //     MMA's B operand), then read each down block and add gate * y into the fp32 output
 //     with coalesced atomics: the weighted combine and the f-split reduction are fused.
+//   * The MMA warp runs one item ahead on gate/up: the order of stages (and of the
+//     producer's loads) is gu(0), gu(1), down(0), gu(2), down(1), ... so the tensor pipe
+//     and the copy engine stay busy while the epilogue turns item j's accumulators into h.
+//     The gate/up accumulators and h are double-buffered by item parity; the down blocks
+//     go through a ring of kDownBufs TMEM accumulators so the MMA warp rarely waits for
+//     the epilogue.
 //   * Every wait is bounded (common.cuh); a time-out raises an abort flag that every role
 //     honours, records MOE_ERR_DEVICE_TIMEOUT, drains copies and MMAs in flight and frees
 //     TMEM before the CTA exits.
@@ -43,15 +49,31 @@ constexpr int kOB = 128;                    // d rows per down block
 constexpr int kNT = 16;                     // MMA N (token columns)
 constexpr uint32_t kStageBytes = 16384;
 constexpr uint32_t kXTileBytes = kNT * 128;   // one k block of x: 16 rows x 128 B
-constexpr uint32_t kHBytes = kNT * 128;
+constexpr uint32_t kHBytes = kNT * 128;       // one h tile (16 rows x 64 bf16)
 constexpr uint32_t kUXBytes = 64 * kNT * 4;
-constexpr uint32_t kTmemCols = 64;          // [0,16) gate/up, [16,32) and [32,48) down
+constexpr int kDownBufs = 8;                // TMEM ring of down-block accumulators
+constexpr uint32_t kColGU = 0;              // [0,16) and [16,32): gate/up, by item parity
+constexpr uint32_t kColDown = 32;           // [32, 32 + 16 * kDownBufs)
+constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kIdesc = idesc_bf16_f32(128, kNT);
-constexpr int kMaxStages = 12;
-constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s
+constexpr int kMaxStages = 8;
+constexpr long long kDrainCycles = 400000000ll;   // about 0.2 s
 
 struct SmemLayout {
     uint32_t x, stages, h, ux, bars, misc, total;
+};
+
+// barrier slots after the 2*stages ring barriers
+enum {
+    kBarX = 0,
+    kBarGU0,
+    kBarGU1,
+    kBarUX,
+    kBarH,
+    kBarDrain,
+    kBarDFull0,
+    kBarDEmpty0 = kBarDFull0 + kDownBufs,
+    kNumMiscBars = kBarDEmpty0 + kDownBufs
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int d, int stages) {
@@ -59,29 +81,36 @@ __host__ __device__ inline SmemLayout smem_layout(int d, int stages) {
     L.x = 0;
     L.stages = L.x + static_cast<uint32_t>(d / kBK) * kXTileBytes;
     L.h = L.stages + static_cast<uint32_t>(stages) * kStageBytes;
-    L.ux = L.h + kHBytes;
+    L.ux = L.h + 2 * kHBytes;
     L.bars = L.ux + kUXBytes;
-    L.misc = L.bars + static_cast<uint32_t>(2 * stages + 10) * 8;
+    L.misc = L.bars + static_cast<uint32_t>(2 * stages + kNumMiscBars) * 8;
     L.total = L.misc + 16;
     return L;
 }
 
-// barrier slots after the 2*stages ring barriers
-enum { kBarX = 0, kBarGU, kBarUX, kBarH, kBarDFull0, kBarDFull1, kBarDEmpty0, kBarDEmpty1, kBarDrain };
-
 struct Item {
-    int e;       // expert, or -1 if the item is skipped
+    int e;       // expert
     int g;       // group
     int i0;      // first row of the f tile
 };
 
-__device__ __forceinline__ Item item_of(const ExpertArgs &a, int it, int tiles) {
-    Item r;
+// Work item it of this call.  Returns false for an item whose expert id is outside
+// [0, N): every role skips those the same way.
+__device__ __forceinline__ bool item_of(const ExpertArgs &a, int it, int tiles, Item &r) {
     r.g = it / tiles;
     r.i0 = (it - r.g * tiles) * kFTile;
-    const int e = (a.mode == kModePerSlot) ? a.ids[r.g] : a.expert_list[r.g];
-    r.e = (e >= 0 && e < a.N) ? e : -1;
-    return r;
+    r.e = (a.mode == kModePerSlot) ? a.ids[r.g] : a.expert_list[r.g];
+    return r.e >= 0 && r.e < a.N;
+}
+
+// The next valid item of this CTA at or after it (static round robin), or -1.
+__device__ __forceinline__ int next_item(const ExpertArgs &a, int it, int items, int tiles, Item &r,
+                                         bool report) {
+    for (; it < items; it += gridDim.x) {
+        if (item_of(a, it, tiles, r)) return it;
+        if (report && r.i0 == 0) record_error(a.err, MOE_ERR_BAD_ID);
+    }
+    return -1;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -102,7 +131,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     uint8_t *const h_ptr = base_ptr + L.h;
     const uint32_t bar_full = base + L.bars;                 // [stages]
     const uint32_t bar_empty = bar_full + 8u * stages;       // [stages]
-    const uint32_t bar_misc = bar_empty + 8u * stages;       // [10]
+    const uint32_t bar_misc = bar_empty + 8u * stages;       // [kNumMiscBars]
     auto bar = [&](int k) { return bar_misc + 8u * static_cast<uint32_t>(k); };
     uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + L.misc);
     volatile int32_t *const abort_flag = reinterpret_cast<volatile int32_t *>(base_ptr + L.misc + 4);
@@ -117,14 +146,15 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             mbar_init(bar_empty + 8u * s, 1);
         }
         mbar_init(bar(kBarX), 1);
-        mbar_init(bar(kBarGU), 1);
+        mbar_init(bar(kBarGU0), 1);
+        mbar_init(bar(kBarGU1), 1);
         mbar_init(bar(kBarUX), 64);
         mbar_init(bar(kBarH), 64);
-        mbar_init(bar(kBarDFull0), 1);
-        mbar_init(bar(kBarDFull1), 1);
-        mbar_init(bar(kBarDEmpty0), 128);
-        mbar_init(bar(kBarDEmpty1), 128);
         mbar_init(bar(kBarDrain), 1);
+        for (int b = 0; b < kDownBufs; ++b) {
+            mbar_init(bar(kBarDFull0 + b), 1);
+            mbar_init(bar(kBarDEmpty0 + b), 128);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_map(&tm_wg);
@@ -155,113 +185,160 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            uint32_t cnt = 0;
-            bool ok = true;
+        // The whole warp walks the schedule and waits; one elected lane issues the copies.
+        uint32_t cnt = 0;
+        bool ok = true;
+        auto acquire = [&](uint32_t &dst, uint32_t &fb, bool &leader) -> bool {
+            const uint32_t s = cnt % stages, ph = (cnt / stages) & 1u;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_empty + 8u * s, ph ^ 1u, abort_flag, a.err))) return false;
+            dst = sstage + s * kStageBytes;
+            fb = bar_full + 8u * s;
+            leader = elect_one();
+            if (leader) mbar_arrive_expect_tx(fb, kStageBytes);
+            ++cnt;
+            return true;
+        };
+        auto load_gu = [&](const Item &im) -> bool {
+            const int row = im.e * a.f + im.i0;
+            for (int kb = 0; kb < KB; ++kb) {
+                uint32_t dst, fb;
+                bool leader;
+                if (!acquire(dst, fb, leader)) return false;
+                if (leader) {
+                    tma_load_2d(dst, &tm_wg, fb, kb * kBK, row);
+                    tma_load_2d(dst + kStageBytes / 2, &tm_wu, fb, kb * kBK, row);
+                }
+                __syncwarp();
+            }
+            return true;
+        };
+        auto load_down = [&](const Item &im) -> bool {
+            for (int ob = 0; ob < OBS; ++ob) {
+                uint32_t dst, fb;
+                bool leader;
+                if (!acquire(dst, fb, leader)) return false;
+                if (leader) tma_load_2d(dst, &tm_wd, fb, im.i0, im.e * a.d + ob * kOB);
+                __syncwarp();
+            }
+            return true;
+        };
+        if (elect_one()) {
             mbar_arrive_expect_tx(bar(kBarX), static_cast<uint32_t>(KB) * kXTileBytes);
             for (int kb = 0; kb < KB; ++kb)
                 tma_load_2d(sx + kb * kXTileBytes, &tm_x, bar(kBarX), kb * kBK, 0);
-            for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
-                const Item im = item_of(a, it, tiles);
-                if (im.e < 0) continue;
-                const int row_gu = im.e * a.f + im.i0;
-                for (int kb = 0; kb < KB; ++kb, ++cnt) {
-                    const uint32_t s = cnt % stages, ph = (cnt / stages) & 1u;
-                    if (!mbar_wait(bar_empty + 8u * s, ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
-                    const uint32_t dst = sstage + s * kStageBytes;
-                    mbar_arrive_expect_tx(bar_full + 8u * s, kStageBytes);
-                    tma_load_2d(dst, &tm_wg, bar_full + 8u * s, kb * kBK, row_gu);
-                    tma_load_2d(dst + kStageBytes / 2, &tm_wu, bar_full + 8u * s, kb * kBK, row_gu);
-                }
-                for (int ob = 0; ok && ob < OBS; ++ob, ++cnt) {
-                    const uint32_t s = cnt % stages, ph = (cnt / stages) & 1u;
-                    if (!mbar_wait(bar_empty + 8u * s, ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
-                    const uint32_t dst = sstage + s * kStageBytes;
-                    mbar_arrive_expect_tx(bar_full + 8u * s, kStageBytes);
-                    tma_load_2d(dst, &tm_wd, bar_full + 8u * s, im.i0, im.e * a.d + ob * kOB);
-                }
-            }
-            if (!ok) {
-                // wait (bounded) for the copies this thread issued and nobody consumed
-                const uint32_t first = cnt > static_cast<uint32_t>(stages) ? cnt - stages : 0u;
-                for (uint32_t j = first; j < cnt; ++j)
-                    mbar_wait_drain(bar_full + 8u * (j % stages), (j / stages) & 1u, kDrainNs);
-                mbar_wait_drain(bar(kBarX), 0, kDrainNs);
-            }
         }
+        __syncwarp();
+        Item cur, nxt;
+        int it = next_item(a, blockIdx.x, items, tiles, cur, false);
+        if (it >= 0) ok = load_gu(cur);
+        while (ok && it >= 0) {
+            const int it2 = next_item(a, it + gridDim.x, items, tiles, nxt, false);
+            if (it2 >= 0) ok = load_gu(nxt);
+            if (ok) ok = load_down(cur);
+            it = it2;
+            cur = nxt;
+        }
+        if (!ok && lane == 0) {
+            // wait (bounded) for the copies this warp issued and nobody consumed
+            const uint32_t first = cnt > static_cast<uint32_t>(stages) ? cnt - stages : 0u;
+            for (uint32_t j = first; j < cnt; ++j)
+                mbar_wait_drain(bar_full + 8u * (j % stages), (j / stages) & 1u, kDrainCycles);
+            mbar_wait_drain(bar(kBarX), 0, kDrainCycles);
+        }
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t cnt = 0, dcnt = 0, nitem = 0;
-            bool ok = mbar_wait(bar(kBarX), 0, abort_flag, a.err);
-            tc_fence_after();
-            for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
-                const Item im = item_of(a, it, tiles);
-                if (im.e < 0) continue;
-                for (int kb = 0; kb < KB; ++kb, ++cnt) {
-                    const uint32_t s = cnt % stages, ph = (cnt / stages) & 1u;
-                    if (!mbar_wait(bar_full + 8u * s, ph, abort_flag, a.err)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t sa = sstage + s * kStageBytes;
-                    const uint32_t sb = sx + kb * kXTileBytes;
-#pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k)
-                        tc_mma_bf16(tmem, desc_kmajor_sw128(sa + 32u * k), desc_kmajor_sw128(sb + 32u * k),
-                                    kIdesc, (kb | k) != 0 ? 1u : 0u);
-                    tc_commit(bar_empty + 8u * s);
-                }
-                if (!ok) break;
-                tc_commit(bar(kBarGU));
-                if (!mbar_wait(bar(kBarH), nitem & 1u, abort_flag, a.err)) { ok = false; break; }
+        // Warp-uniform loop; waits by every lane, MMAs and commits by one elected lane.
+        uint32_t cnt = 0, dcnt = 0, nitem = 0;
+        bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarX), 0, abort_flag, a.err));
+        tc_fence_after();
+        auto mma_gu = [&](uint32_t gbuf) -> bool {
+            for (int kb = 0; kb < KB; ++kb, ++cnt) {
+                const uint32_t s = cnt % stages, ph = (cnt / stages) & 1u;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_full + 8u * s, ph, abort_flag, a.err))) return false;
                 tc_fence_after();
-                for (int ob = 0; ob < OBS; ++ob, ++cnt, ++dcnt) {
-                    const uint32_t s = cnt % stages, ph = (cnt / stages) & 1u;
-                    const uint32_t buf = dcnt & 1u, dph = (dcnt >> 1) & 1u;
-                    if (!mbar_wait(bar_full + 8u * s, ph, abort_flag, a.err)) { ok = false; break; }
-                    if (!mbar_wait(bar(kBarDEmpty0 + buf), dph ^ 1u, abort_flag, a.err)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t sa = sstage + s * kStageBytes;
+                const uint32_t sa = sstage + s * kStageBytes;
+                const uint32_t sb = sx + kb * kXTileBytes;
+                if (elect_one()) {
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k)
-                        tc_mma_bf16(tmem + 16u + 16u * buf, desc_kmajor_sw128(sa + 32u * k),
-                                    desc_kmajor_sw128(sh + 32u * k), kIdesc, k != 0 ? 1u : 0u);
+                        tc_mma_bf16(tmem + kColGU + 16u * gbuf, desc_kmajor_sw128(sa + 32u * k),
+                                    desc_kmajor_sw128(sb + 32u * k), kIdesc, (kb | k) != 0 ? 1u : 0u);
+                    tc_commit(bar_empty + 8u * s);
+                    if (kb == KB - 1) tc_commit(bar(kBarGU0 + gbuf));
+                }
+                __syncwarp();
+            }
+            return true;
+        };
+        auto mma_down = [&](uint32_t hbuf) -> bool {
+            for (int ob = 0; ob < OBS; ++ob, ++cnt, ++dcnt) {
+                const uint32_t s = cnt % stages, ph = (cnt / stages) & 1u;
+                const uint32_t buf = dcnt % kDownBufs, dph = (dcnt / kDownBufs) & 1u;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_full + 8u * s, ph, abort_flag, a.err))) return false;
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarDEmpty0 + buf), dph ^ 1u, abort_flag, a.err)))
+                    return false;
+                tc_fence_after();
+                const uint32_t sa = sstage + s * kStageBytes;
+                const uint32_t sb = sh + hbuf * kHBytes;
+                if (elect_one()) {
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k)
+                        tc_mma_bf16(tmem + kColDown + 16u * buf, desc_kmajor_sw128(sa + 32u * k),
+                                    desc_kmajor_sw128(sb + 32u * k), kIdesc, k != 0 ? 1u : 0u);
                     tc_commit(bar_empty + 8u * s);
                     tc_commit(bar(kBarDFull0 + buf));
                 }
-                ++nitem;
+                __syncwarp();
             }
-            // every MMA this thread issued completes before TMEM is released
-            tc_commit(bar(kBarDrain));
-            mbar_wait_drain(bar(kBarDrain), 0, kDrainNs);
+            return true;
+        };
+        Item cur, nxt;
+        int it = next_item(a, blockIdx.x, items, tiles, cur, false);
+        if (ok && it >= 0) ok = mma_gu(0);
+        while (ok && it >= 0) {
+            const int it2 = next_item(a, it + gridDim.x, items, tiles, nxt, false);
+            if (it2 >= 0) ok = mma_gu((nitem + 1) & 1u);
+            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarH), nitem & 1u, abort_flag, a.err));
+            if (ok) {
+                tc_fence_after();
+                ok = mma_down(nitem & 1u);
+            }
+            ++nitem;
+            it = it2;
         }
+        // every MMA this warp issued completes before TMEM is released
+        if (elect_one()) {
+            tc_commit(bar(kBarDrain));
+            mbar_wait_drain(bar(kBarDrain), 0, kDrainCycles);
+        }
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;               // TMEM lane quarter of this warp
         const int row = q * 32 + lane;        // TMEM lane = accumulator row
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const bool reporter = (warp == 2 && lane == 0);
         uint32_t dcnt = 0, nitem = 0;
         bool ok = true;
-        for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
-            const Item im = item_of(a, it, tiles);
-            if (im.e < 0) {
-                if (row == 0 && im.i0 == 0) record_error(a.err, MOE_ERR_BAD_ID);
-                continue;
-            }
+        Item cur;
+        for (int it = next_item(a, blockIdx.x, items, tiles, cur, reporter); ok && it >= 0;
+             it = next_item(a, it + gridDim.x, items, tiles, cur, reporter), ++nitem) {
             // gate of each pass token in this group (0 if absent)
             float gt[kNT];
 #pragma unroll
             for (int t = 0; t < kNT; ++t) gt[t] = 0.0f;
             uint32_t mask = 0;
             if (a.mode == kModePerSlot) {
-                const int tt = im.g / a.m;
-                const float gv = a.gates[im.g];
+                const int tt = cur.g / a.m;
+                const float gv = a.gates[cur.g];
 #pragma unroll
                 for (int t = 0; t < kNT; ++t)
                     if (t == tt) gt[t] = gv;
                 mask = 1u << tt;
             } else {
                 const int S = a.n * a.m;   // offsets are clamped to the slot buffer
-                const int p0 = max(0, a.offsets[im.g]), p1 = min(S, a.offsets[im.g + 1]);
+                const int p0 = max(0, a.offsets[cur.g]), p1 = min(S, a.offsets[cur.g + 1]);
                 for (int p = p0; p < p1; ++p) {
                     const int slot = a.slot_order[p];
                     const int tt = slot / a.m;
@@ -274,15 +351,17 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 }
             }
 
-            // gate/up accumulators -> h (bf16, swizzled B operand of the down MMA)
-            // outcomes are made warp-uniform so the .sync.aligned TMEM loads stay converged
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarGU), nitem & 1u, abort_flag, a.err))) {
+            // gate/up accumulators -> h (bf16, swizzled B operand of the down MMA).
+            // Wait outcomes are made warp-uniform so the .sync.aligned TMEM loads stay
+            // converged.
+            const uint32_t gbuf = nitem & 1u;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarGU0 + gbuf), (nitem >> 1) & 1u, abort_flag, a.err))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             float v[16];
-            tmem_ld_16(tmem + lane_off, v);
+            tmem_ld_16(tmem + lane_off + kColGU + 16u * gbuf, v);
             if (q >= 2) {
                 const int r = row - 64;
 #pragma unroll
@@ -295,12 +374,13 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                     break;
                 }
                 const int i = row;   // 0..63
+                uint8_t *const hb = h_ptr + gbuf * kHBytes;
 #pragma unroll
                 for (int c = 0; c < kNT; ++c) {
                     const float hv = silu(v[c]) * ux[c * 64 + i];
                     const uint32_t off = static_cast<uint32_t>((c >> 3) * 1024 + (c & 7) * 128 +
                                                                ((((i >> 3) ^ (c & 7))) << 4) + (i & 7) * 2);
-                    *reinterpret_cast<__nv_bfloat16 *>(h_ptr + off) = __float2bfloat16_rn(hv);
+                    *reinterpret_cast<__nv_bfloat16 *>(hb + off) = __float2bfloat16_rn(hv);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -309,13 +389,13 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
 
             // down blocks: y[t, o] += gate_t * Y[o, t]
             for (int ob = 0; ob < OBS; ++ob, ++dcnt) {
-                const uint32_t buf = dcnt & 1u, dph = (dcnt >> 1) & 1u;
+                const uint32_t buf = dcnt % kDownBufs, dph = (dcnt / kDownBufs) & 1u;
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarDFull0 + buf), dph, abort_flag, a.err))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                tmem_ld_16(tmem + lane_off + 16u + 16u * buf, v);
+                tmem_ld_16(tmem + lane_off + kColDown + 16u * buf, v);
                 tc_fence_before();
                 mbar_arrive(bar(kBarDEmpty0 + buf));
                 const int o = ob * kOB + row;
@@ -323,7 +403,6 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 for (int t = 0; t < kNT; ++t)
                     if ((mask >> t) & 1u) atomicAdd(a.y + static_cast<size_t>(t) * a.d + o, gt[t] * v[t]);
             }
-            ++nitem;
         }
     }
 
