@@ -86,12 +86,12 @@ const char *moe_status_str(moe_status_t status);
 
 /*
  * Bytes of device workspace the expert-operation calls need for this layer and passes
- * of up to n_max tokens.  The workspace holds the device error word; it must be zeroed
- * once with moe_workspace_init before its first use.
+ * of up to n_max tokens.  The workspace holds the device error word; zero it once with
+ * moe_workspace_init before its first use.
  */
 size_t moe_workspace_bytes(const moe_layer_t *layer, int32_t n_max);
 
-/* Zeroes the workspace [dev] (ws_bytes >= moe_workspace_bytes) on stream s. */
+/* Zeroes all ws_bytes of the workspace [dev] on stream s. */
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t s);
 
 /*

@@ -119,7 +119,7 @@ size_t moe_workspace_bytes(const moe_layer_t *layer, int32_t n_max) {
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t s) {
     if (ws == nullptr || ws_bytes < kWorkspaceBytes) return MOE_ERR_WORKSPACE;
     if (!aligned16(ws)) return MOE_ERR_ARG;
-    return cuda_status(cudaMemsetAsync(ws, 0, kWorkspaceBytes, reinterpret_cast<cudaStream_t>(s)));
+    return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, reinterpret_cast<cudaStream_t>(s)));
 }
 
 moe_status_t moe_route_topm(const float *logits, int32_t n, int32_t N, int32_t m, int32_t renorm, int32_t *ids,

@@ -56,7 +56,7 @@ constexpr uint32_t kColGU = 0;              // [0,16) and [16,32): gate/up, by i
 constexpr uint32_t kColDown = 32;           // [32, 32 + 16 * kDownBufs)
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kIdesc = idesc_bf16_f32(128, kNT);
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 9;
 constexpr long long kDrainCycles = 400000000ll;   // about 0.2 s
 
 struct SmemLayout {
@@ -65,8 +65,7 @@ struct SmemLayout {
 
 // barrier slots after the 2*stages ring barriers
 enum {
-    kBarX = 0,
-    kBarGU0,
+    kBarGU0 = 0,
     kBarGU1,
     kBarUX,
     kBarH,
@@ -145,7 +144,6 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             mbar_init(bar_full + 8u * s, 1);
             mbar_init(bar_empty + 8u * s, 1);
         }
-        mbar_init(bar(kBarX), 1);
         mbar_init(bar(kBarGU0), 1);
         mbar_init(bar(kBarGU1), 1);
         mbar_init(bar(kBarUX), 64);
@@ -188,46 +186,45 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         // The whole warp walks the schedule and waits; one elected lane issues the copies.
         uint32_t cnt = 0;
         bool ok = true;
-        auto acquire = [&](uint32_t &dst, uint32_t &fb, bool &leader) -> bool {
+        auto acquire = [&](uint32_t &dst, uint32_t &fb, bool &leader, uint32_t extra) -> bool {
             const uint32_t s = cnt % stages, ph = (cnt / stages) & 1u;
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_empty + 8u * s, ph ^ 1u, abort_flag, a.err))) return false;
             dst = sstage + s * kStageBytes;
             fb = bar_full + 8u * s;
             leader = elect_one();
-            if (leader) mbar_arrive_expect_tx(fb, kStageBytes);
+            if (leader) mbar_arrive_expect_tx(fb, kStageBytes + extra);
             ++cnt;
             return true;
         };
+        // The first gate/up item also brings the pass's x, one 2 KB k block per stage, so
+        // the first weights arrive without waiting behind the whole of x.
+        bool x_pending = true;
         auto load_gu = [&](const Item &im) -> bool {
             const int row = im.e * a.f + im.i0;
             for (int kb = 0; kb < KB; ++kb) {
                 uint32_t dst, fb;
                 bool leader;
-                if (!acquire(dst, fb, leader)) return false;
+                if (!acquire(dst, fb, leader, x_pending ? kXTileBytes : 0u)) return false;
                 if (leader) {
                     tma_load_2d(dst, &tm_wg, fb, kb * kBK, row);
                     tma_load_2d(dst + kStageBytes / 2, &tm_wu, fb, kb * kBK, row);
+                    if (x_pending) tma_load_2d(sx + kb * kXTileBytes, &tm_x, fb, kb * kBK, 0);
                 }
                 __syncwarp();
             }
+            x_pending = false;
             return true;
         };
         auto load_down = [&](const Item &im) -> bool {
             for (int ob = 0; ob < OBS; ++ob) {
                 uint32_t dst, fb;
                 bool leader;
-                if (!acquire(dst, fb, leader)) return false;
+                if (!acquire(dst, fb, leader, 0u)) return false;
                 if (leader) tma_load_2d(dst, &tm_wd, fb, im.i0, im.e * a.d + ob * kOB);
                 __syncwarp();
             }
             return true;
         };
-        if (elect_one()) {
-            mbar_arrive_expect_tx(bar(kBarX), static_cast<uint32_t>(KB) * kXTileBytes);
-            for (int kb = 0; kb < KB; ++kb)
-                tma_load_2d(sx + kb * kXTileBytes, &tm_x, bar(kBarX), kb * kBK, 0);
-        }
-        __syncwarp();
         Item cur, nxt;
         int it = next_item(a, blockIdx.x, items, tiles, cur, false);
         if (it >= 0) ok = load_gu(cur);
@@ -243,15 +240,13 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             const uint32_t first = cnt > static_cast<uint32_t>(stages) ? cnt - stages : 0u;
             for (uint32_t j = first; j < cnt; ++j)
                 mbar_wait_drain(bar_full + 8u * (j % stages), (j / stages) & 1u, kDrainCycles);
-            mbar_wait_drain(bar(kBarX), 0, kDrainCycles);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // Warp-uniform loop; waits by every lane, MMAs and commits by one elected lane.
         uint32_t cnt = 0, dcnt = 0, nitem = 0;
-        bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarX), 0, abort_flag, a.err));
-        tc_fence_after();
+        bool ok = true;
         auto mma_gu = [&](uint32_t gbuf) -> bool {
             for (int kb = 0; kb < KB; ++kb, ++cnt) {
                 const uint32_t s = cnt % stages, ph = (cnt / stages) & 1u;
@@ -365,7 +360,8 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             if (q >= 2) {
                 const int r = row - 64;
 #pragma unroll
-                for (int c = 0; c < kNT; ++c) ux[c * 64 + r] = v[c];
+                for (int c = 0; c < kNT; ++c)
+                    if ((mask >> c) & 1u) ux[c * 64 + r] = v[c];
                 tc_fence_before();
                 mbar_arrive(bar(kBarUX));
             } else {
@@ -377,6 +373,8 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 uint8_t *const hb = h_ptr + gbuf * kHBytes;
 #pragma unroll
                 for (int c = 0; c < kNT; ++c) {
+                    // columns of tokens outside the group are never read back: skip them
+                    if (!((mask >> c) & 1u)) continue;
                     const float hv = silu(v[c]) * ux[c * 64 + i];
                     const uint32_t off = static_cast<uint32_t>((c >> 3) * 1024 + (c & 7) * 128 +
                                                                ((((i >> 3) ^ (c & 7))) << 4) + (i & 7) * 2);
