@@ -482,12 +482,14 @@ def run_reference(args, world, rank):
     oracle.build()
     wl = BY_NAME[args.workload]
     n_max = args.n_max or max(wl.n_values)
-    wg, wu, wd = synth.expert_weights(wl.N, wl.f, wl.d, torch.bfloat16, synth.seed_for(wl.index, layer=0))
+    dt = torch.bfloat16 if wl.w_dtype == "bf16" else torch.float32
+    wg, wu, wd = synth.expert_weights(wl.N, wl.f, wl.d, dt, synth.seed_for(wl.index, layer=0))
     host_w = tuple(synth.host_array(t) for t in (wg, wu, wd))
     T = (args.warmup + args.steps) * n_max
     sets, _ = synth.routing_traces(1, T, wl.N, wl.m, wl.rhos[0], seed=synth.seed_for(wl.index, stream=2))
-    x_host = synth.host_array(synth.activations(n_max, wl.d, torch.bfloat16, seed=synth.seed_for(wl.index, stream=1)))
-    n_step = [1 + (k * 5) % n_max for k in range(args.warmup + args.steps)]   # cycle over pass sizes
+    x_host = synth.host_array(synth.activations(n_max, wl.d, dt, seed=synth.seed_for(wl.index, stream=1)))
+    n_step = [min(wl.n_values) + (k * 5) % (n_max - min(wl.n_values) + 1)
+              for k in range(args.warmup + args.steps)]   # cycle over pass sizes
     for k in range(args.warmup):
         _oracle_sample(oracle, wl, host_w, sets[0][k * n_max:], x_host, [n_step[k]], budget_s=1e9)
     nb_tot, s_tot = 0, 0.0
@@ -498,22 +500,24 @@ def run_reference(args, world, rank):
     value = nb_tot / s_tot / 1e12
     sample = (f"one layer of {wl.name}, one pass per step at n in {n_step[args.warmup:]}, "
               f"per-slot and dedup forms, single-threaded fp64 C oracle")
-    line = dict(metric=METRIC, value=round(value, 8), unit=UNIT, n_gpus=world, steps=args.steps,
+    line = dict(metric=METRIC, value=round(value, 10), unit=UNIT, n_gpus=world, steps=args.steps,
                 warmup=args.warmup, ms_per_step=round(s_tot / args.steps * 1e3, 1), higher_is_better=True,
                 scaling="weak", vs_baseline=None, dtype="f64", data="synthetic", impl="reference",
                 config=dict(workload=wl.name, layers=1, d=wl.d, f=wl.f, N=wl.N, m=wl.m, rho=wl.rhos[0]),
-                cpu_baseline=dict(value=round(value, 8), unit=UNIT, cores=1, kind="oracle", sample=sample),
-                e2e=dict(value=round(value, 8), unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+                cpu_baseline=dict(value=round(value, 10), unit=UNIT, cores=1, kind="oracle", sample=sample),
+                e2e=dict(value=round(value, 10), unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(line), flush=True)
 
 
 def main():
     args = parse()
-    world, rank, local = dist_setup(args)
     if args.impl == "reference":
-        run_reference(args, world, rank)
-    else:
-        run_ours(args, world, rank, local)
+        # the oracle needs no collective: rank 0 runs it, other ranks exit without work
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        run_reference(args, world, int(os.environ.get("RANK", "0")))
+        return
+    world, rank, local = dist_setup(args)
+    run_ours(args, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
