@@ -171,6 +171,30 @@ moe_status_t moe_expert_op_dedup(const moe_layer_t *layer, const void *w_gate, c
                                  moe_stream_t s);
 
 /*
+ * The per-slot expert operation without a caller workspace.  The paper has no
+ * counterpart: this is a service to callers that cannot allocate device memory -- code
+ * running under a memory manager that owns every device byte (a serving framework's
+ * caching allocator, a fixed arena budgeted ahead of time), where a raw cudaMalloc would
+ * bypass its accounting, and code on a latency-critical path, where cudaMalloc and
+ * cudaFree synchronise the device.  It allocates nothing and calls no allocating routine.
+ *   Arguments and results as moe_expert_op_perslot, without ws/ws_bytes, plus
+ *   status_out [dev] int32 [1] or NULL: receives the call's device error word (MOE_OK,
+ *   MOE_ERR_BAD_ID or MOE_ERR_DEVICE_TIMEOUT), written on stream s after the kernels.
+ * Scratch: a 256-byte array inside the library, held by every GPU that loads it until the
+ * process exits.  A layer or pass whose workspace (moe_workspace_bytes) would exceed it is
+ * rejected with MOE_ERR_WORKSPACE.  The array is cleared at the start of every call and
+ * keeps the last call's contents after it.  All calls on a GPU share it, so calls that
+ * overlap on that GPU (on different streams, or from different host threads) race: order
+ * them on one stream.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current and caches it; make that first call before any stream capture.
+ */
+moe_status_t moe_expert_op_perslot_noalloc(const moe_layer_t *layer, const void *w_gate, const void *w_up,
+                                           const void *w_down, const void *x, const int32_t *ids,
+                                           const float *gates, int32_t n, int32_t accumulate, float *y,
+                                           int32_t *status_out, moe_stream_t s);
+
+/*
  * Requested bytes of one pass [Lan, §1 "Bytes": E_slot = m*n*w, E_dedup = w * X(n);
  * §2 "Effective bandwidth": u_bar(n) = E_dedup / E_slot].  Host only.
  *   ids_host [host] int32 [n*m].

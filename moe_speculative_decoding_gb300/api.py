@@ -49,7 +49,7 @@ class _PassBytes(ctypes.Structure):
 EXPORTED = ("moe_abi_version", "moe_status_str", "moe_workspace_bytes", "moe_workspace_init",
             "moe_route_topm", "moe_group_slots", "moe_expert_op_perslot", "moe_expert_op_dedup",
             "moe_pass_bytes", "moe_bandwidth_report", "moe_expected_union",
-            "moe_best_draft_length", "moe_last_device_error")
+            "moe_best_draft_length", "moe_last_device_error", "moe_expert_op_perslot_noalloc")
 
 _lib = None
 
