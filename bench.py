@@ -160,9 +160,11 @@ def kernel_traffic(kernel: str):
     if not ent:
         return None
     import hashlib
-    src = os.path.join(ROOT, ent["source"])
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    if digest != ent.get("source_sha256"):
+    h = hashlib.sha256()
+    for src in ent["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != ent.get("sources_sha256"):
         return None
     return ent
 
