@@ -86,8 +86,12 @@ const char *moe_status_str(moe_status_t status);
 
 /*
  * Bytes of device workspace the expert-operation calls need for this layer and passes
- * of up to n_max tokens.  The workspace holds the device error word; zero it once with
- * moe_workspace_init before its first use.
+ * of up to n_max tokens: 256 bytes holding the device error word and, for layers the bf16
+ * tensor-core path runs, the fp32 gate/up partial sums its two kernels hand over,
+ * 3 * 128 * 4 bytes per (slot, 64-row tile of f): 256 + n_max*m*(f/64)*1536 bytes
+ * (2.4 MB for d = 2048, f = 768, top-8 at 16 tokens).  Zero it once with
+ * moe_workspace_init before its first use; calls rewrite the partial sums before they
+ * read them.  n_max above MOE_MAX_PASS_TOKENS counts as MOE_MAX_PASS_TOKENS.
  */
 size_t moe_workspace_bytes(const moe_layer_t *layer, int32_t n_max);
 
@@ -180,10 +184,10 @@ moe_status_t moe_expert_op_dedup(const moe_layer_t *layer, const void *w_gate, c
  *   Arguments and results as moe_expert_op_perslot, without ws/ws_bytes, plus
  *   status_out [dev] int32 [1] or NULL: receives the call's device error word (MOE_OK,
  *   MOE_ERR_BAD_ID or MOE_ERR_DEVICE_TIMEOUT), written on stream s after the kernels.
- * Scratch: a 256-byte array inside the library, held by every GPU that loads it until the
+ * Scratch: a 16 MiB array inside the library, held by every GPU that loads it until the
  * process exits.  A layer or pass whose workspace (moe_workspace_bytes) would exceed it is
- * rejected with MOE_ERR_WORKSPACE.  The array is cleared at the start of every call and
- * keeps the last call's contents after it.  All calls on a GPU share it, so calls that
+ * rejected with MOE_ERR_WORKSPACE.  Its error word is cleared at the start of every call,
+ * and the array keeps the last call's contents after it.  All calls on a GPU share it, so calls that
  * overlap on that GPU (on different streams, or from different host threads) race: order
  * them on one stream.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress)

@@ -29,6 +29,12 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// the bf16 tensor-core path runs this layer (else the SIMT kernel)
+bool uses_tc(const moe_layer_t *L) {
+    return L->w_dtype == MOE_BF16 && L->x_dtype == MOE_BF16 && !(L->flags & MOE_FLAG_SIMT) &&
+           expert_tc_supports(L->d, L->f);
+}
+
 moe_status_t check_layer(const moe_layer_t *L) {
     if (L == nullptr) return MOE_ERR_ARG;
     if (L->d <= 0 || L->f <= 0 || L->N <= 0 || L->m <= 0) return MOE_ERR_ARG;
@@ -51,7 +57,7 @@ moe_status_t check_expert_common(const moe_layer_t *L, const void *wg, const voi
     const void *ptrs[] = {wg, wu, wd, x, gates, y};
     for (const void *p : ptrs)
         if (p == nullptr || !aligned16(p)) return MOE_ERR_ARG;
-    if (ws == nullptr || ws_bytes < kWorkspaceBytes) return MOE_ERR_WORKSPACE;
+    if (ws == nullptr || ws_bytes < moe_workspace_bytes(L, n)) return MOE_ERR_WORKSPACE;
     if (!aligned16(ws)) return MOE_ERR_ARG;
     return MOE_OK;
 }
@@ -78,14 +84,18 @@ ExpertArgs make_args(const moe_layer_t *L, const void *wg, const void *wu, const
     return a;
 }
 
-moe_status_t run_expert(const moe_layer_t *L, const ExpertArgs &a, int max_groups, int32_t accumulate,
+moe_status_t run_expert(const moe_layer_t *L, const ExpertArgs &a, int max_groups, int32_t accumulate, void *ws,
                         cudaStream_t s) {
-    if (!accumulate) {
-        cudaError_t e = cudaMemsetAsync(a.y, 0, sizeof(float) * static_cast<size_t>(a.n) * a.d, s);
-        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    cudaError_t e;
+    if (uses_tc(L)) {
+        // the partial sums live after the workspace header; the gate/up kernel zeroes y
+        float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kWorkspaceBytes);
+        e = launch_expert_tc(a, max_groups, !accumulate, part, s, kUsePdl);
+    } else {
+        e = cudaSuccess;
+        if (!accumulate) e = cudaMemsetAsync(a.y, 0, sizeof(float) * static_cast<size_t>(a.n) * a.d, s);
+        if (e == cudaSuccess) e = launch_expert_simt(a, max_groups, s, kUsePdl);
     }
-    const bool use_tc = L->w_dtype == MOE_BF16 && !(L->flags & MOE_FLAG_SIMT) && expert_tc_supports(L->d, L->f);
-    cudaError_t e = use_tc ? launch_expert_tc(a, max_groups, s, kUsePdl) : launch_expert_simt(a, max_groups, s, kUsePdl);
     if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
     if (e == cudaSuccess) e = cudaGetLastError();
     return cuda_status(e);
@@ -111,9 +121,10 @@ const char *moe_status_str(moe_status_t status) {
 }
 
 size_t moe_workspace_bytes(const moe_layer_t *layer, int32_t n_max) {
-    (void)layer;
-    (void)n_max;
-    return kWorkspaceBytes;
+    if (check_layer(layer) != MOE_OK || n_max < 1 || !uses_tc(layer)) return kWorkspaceBytes;
+    const int n = n_max < MOE_MAX_PASS_TOKENS ? n_max : MOE_MAX_PASS_TOKENS;
+    const size_t part = expert_tc_partial_bytes(layer->f, layer->m, n);
+    return kWorkspaceBytes + (part + 255) / 256 * 256;
 }
 
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t s) {
@@ -159,7 +170,7 @@ moe_status_t moe_expert_op_perslot(const moe_layer_t *layer, const void *w_gate,
     if (ids == nullptr || !aligned16(ids)) return MOE_ERR_ARG;
     ExpertArgs a = make_args(layer, w_gate, w_up, w_down, x, gates, n, y, ws, kModePerSlot);
     a.ids = ids;
-    return run_expert(layer, a, n * layer->m, accumulate, reinterpret_cast<cudaStream_t>(s));
+    return run_expert(layer, a, n * layer->m, accumulate, ws, reinterpret_cast<cudaStream_t>(s));
 }
 
 moe_status_t moe_expert_op_dedup(const moe_layer_t *layer, const void *w_gate, const void *w_up,
@@ -178,7 +189,7 @@ moe_status_t moe_expert_op_dedup(const moe_layer_t *layer, const void *w_gate, c
     a.offsets = expert_offsets;
     a.slot_order = slot_order;
     const int cap = n * layer->m < layer->N ? n * layer->m : layer->N;
-    return run_expert(layer, a, cap, accumulate, reinterpret_cast<cudaStream_t>(s));
+    return run_expert(layer, a, cap, accumulate, ws, reinterpret_cast<cudaStream_t>(s));
 }
 
 moe_status_t moe_pass_bytes(const moe_layer_t *layer, const int32_t *ids_host, int32_t n, moe_pass_bytes_t *out) {

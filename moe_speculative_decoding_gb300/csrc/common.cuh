@@ -96,6 +96,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Warp-wide forms for warp-uniform code.  Every lane polls and acquires for itself (one
+// polling lane with a broadcast measured slower on GB300), and the outcome is made uniform
+// so that .sync.aligned instructions after it stay converged.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int32_t *abort, int32_t *err) {
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort, err));
+}
+// One arrival for the whole warp, after every lane's earlier work (barrier counts are in warps).
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Bounded wait that ignores the abort flag (used to drain copies in flight on abort).
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, long long limit_cycles) {
     const long long t0 = clock64();
@@ -164,6 +176,21 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                      bar)
                  : "memory");
 }
+
+// Each thread of the warp reads 16 consecutive 32-bit columns of its own TMEM lane into
+// raw registers; the values may be used only after tmem_wait_ld().  Several loads in flight
+// share one wait.
+__device__ __forceinline__ void tmem_ld_16_async(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Each thread of the warp reads 16 consecutive 32-bit columns of its own TMEM lane.
 __device__ __forceinline__ void tmem_ld_16(uint32_t taddr, float (&v)[16]) {

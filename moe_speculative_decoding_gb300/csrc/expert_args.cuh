@@ -33,9 +33,18 @@ struct ExpertArgs {
 
 cudaError_t launch_expert_simt(const ExpertArgs &a, int groups, cudaStream_t s, bool pdl);
 
-// Tensor-core kernel (bf16).  Returns cudaErrorNotSupported when the shape is outside
-// what it handles (the caller then reports MOE_ERR_UNSUPPORTED).
-cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, cudaStream_t s, bool pdl);
+// Tensor-core path (bf16): a gate/up kernel and a down kernel.  The gate/up kernel's CTAs
+// share each (group, f tile) item's k blocks, at most kMaxSpan CTAs to an item, and hand
+// their fp32 partial sums to the down kernel through `part`: kMaxSpan * 128 floats per
+// (slot position, f tile), expert_tc_partial_bytes in all.  zero_y: y is overwritten
+// (zeroed by the gate/up kernel) rather than added to.  Returns cudaErrorNotSupported
+// when the shape is outside what it handles (the caller then reports MOE_ERR_UNSUPPORTED).
+constexpr int kMaxSpan = 3;
+inline size_t expert_tc_partial_bytes(int f, int m, int n) {
+    return static_cast<size_t>(n) * m * (f / kFTile) * kMaxSpan * 128 * sizeof(float);
+}
+cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, float *part, cudaStream_t s,
+                             bool pdl);
 bool expert_tc_supports(int d, int f);
 
 }  // namespace moe

@@ -12,10 +12,12 @@
 
 namespace {
 
-// The scratch of moe_expert_op_perslot_noalloc: a workspace of the largest size the
-// per-slot call needs (its device error word).  Every GPU that loads the library holds
-// these bytes until the process exits, and every call of the entry point shares them.
-constexpr size_t kNoAllocScratchBytes = 256;
+// The scratch of moe_expert_op_perslot_noalloc: a workspace (the device error word, then
+// the gate/up partial sums of the tensor-core path) for every layer whose workspace fits
+// 16 MiB, e.g. d = 4096, f = 14336, top-2 at 16 tokens (11 MB).  Every GPU that loads the
+// library holds these bytes until the process exits, and every call of the entry point
+// shares them.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 static_assert(kNoAllocScratchBytes >= moe::kWorkspaceBytes, "scratch smaller than a workspace");
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -55,8 +57,9 @@ extern "C" moe_status_t moe_expert_op_perslot_noalloc(const moe_layer_t *layer, 
     void *ws = nullptr;
     if (scratch_address(&ws) != cudaSuccess) return MOE_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
-    // the previous call's error word must not leak into this one
-    if (cudaMemsetAsync(ws, 0, kNoAllocScratchBytes, st) != cudaSuccess) return MOE_ERR_CUDA;
+    // the previous call's error word must not leak into this one; the partial sums are
+    // written before they are read and need no clearing
+    if (cudaMemsetAsync(ws, 0, moe::kWorkspaceBytes, st) != cudaSuccess) return MOE_ERR_CUDA;
     const moe_status_t r = moe_expert_op_perslot(layer, w_gate, w_up, w_down, x, ids, gates, n, accumulate, y, ws,
                                                  kNoAllocScratchBytes, s);
     if (r != MOE_OK) return r;

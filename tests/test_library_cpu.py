@@ -58,7 +58,38 @@ def test_argument_validation_before_any_launch(lib):
     assert lib.moe_expert_op_dedup(ctypes.byref(mixed), *[None] * 5, 4, *[None] * 4, 0, None, None, 0,
                                    None) == 2
     assert lib.moe_workspace_init(None, 256, None) == 4
-    assert lib.moe_workspace_bytes(ctypes.byref(L), 16) >= 4
+
+
+def test_workspace_bytes(lib):
+    """256 header bytes, plus for the bf16 tensor-core path 3 CTA shares x 128 fp32 partial
+    sums per (slot, 64-row f tile): the gate/up kernel's hand-off to the down kernel."""
+    for (d, f, N, m) in [(2048, 768, 128, 8), (2048, 1408, 64, 6), (4096, 14336, 8, 2), (256, 128, 8, 2)]:
+        L = api.make_layer(d, f, N, m, "bf16")
+        for n in (1, 5, 16):
+            part = n * m * (f // 64) * 3 * 128 * 4
+            assert lib.moe_workspace_bytes(ctypes.byref(L), n) == 256 + (part + 255) // 256 * 256
+        # passes cap at MOE_MAX_PASS_TOKENS
+        assert lib.moe_workspace_bytes(ctypes.byref(L), 64) == lib.moe_workspace_bytes(ctypes.byref(L), 16)
+    assert lib.moe_workspace_bytes(ctypes.byref(api.make_layer(2048, 768, 128, 8)), 16) == 256 + 2359296
+    # the SIMT kernel and fp32 layers keep only the header
+    assert lib.moe_workspace_bytes(ctypes.byref(api.make_layer(256, 512, 8, 2, "f32")), 16) == 256
+    assert lib.moe_workspace_bytes(ctypes.byref(api.make_layer(256, 512, 8, 2, "bf16", simt=True)), 16) == 256
+    assert lib.moe_workspace_bytes(None, 16) == 256
+
+
+def test_noalloc_rejects_layers_beyond_its_scratch(lib):
+    """The 16 MiB library scratch holds 11 MB for d=4096, f=14336, top-2 at 16 tokens; a
+    layer needing more is refused before any device work (no GPU needed for that)."""
+    fn = lib.moe_expert_op_perslot_noalloc
+    P, I32 = ctypes.c_void_p, ctypes.c_int32
+    fn.argtypes = [ctypes.POINTER(api.Layer), P, P, P, P, P, P, I32, I32, P, P, P]
+    fn.restype = I32
+    big = api.make_layer(4096, 65536, 128, 64)   # 16 * 64 * 1024 * 1536 bytes of partial sums
+    assert lib.moe_workspace_bytes(ctypes.byref(big), 16) > 16 << 20
+    assert fn(ctypes.byref(big), *[None] * 6, 16, 0, None, None, None) == 4   # MOE_ERR_WORKSPACE
+    assert fn(None, *[None] * 6, 1, 0, None, None, None) == 1
+    mixtral = api.make_layer(4096, 14336, 8, 2)
+    assert lib.moe_workspace_bytes(ctypes.byref(mixtral), 16) <= 16 << 20
 
 
 def test_pass_bytes_matches_oracle(lib, oracle_mod):
