@@ -55,8 +55,8 @@ constexpr uint32_t kWBytes = 16384;           // weight bytes of one block
 constexpr uint32_t kXTileBytes = kNT * 128;   // x of one k slice: 16 rows x 128 B
 constexpr uint32_t kGUStageBytes = kWBytes + kXTileBytes;
 constexpr uint32_t kHBytes = kNT * 128;       // one h tile: 16 rows x 64 bf16
-constexpr int kGUStages = 6;
-constexpr int kDownStages = 6;
+constexpr int kGUStages = 7;
+constexpr int kDownStages = 5;
 constexpr int kDownBufs = 8;                  // TMEM ring of down-block accumulators
 constexpr int kEpiBatch = 4;                  // down blocks per epilogue round
 constexpr uint32_t kGUTmemCols = 32;          // two 16-column accumulators
@@ -70,11 +70,20 @@ constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr uint32_t kGUBars = kGUStages * kGUStageBytes;
 constexpr uint32_t kGUNumBars = 2 * kGUStages + 5;
 constexpr uint32_t kGUMisc = kGUBars + 8 * kGUNumBars;
-constexpr uint32_t kGUSmem = kGUMisc + 16 + 1024;   // + alignment slack of the base
+constexpr uint32_t kSmemPerSM = 233472;             // shared memory of one SM (228 KB)
+constexpr uint32_t kSmemReserved = 1024;            // reserved by the system per CTA
+// A gate/up CTA takes more than half an SM, so two of them never share one: every SM then
+// keeps room for one down CTA beside its gate/up CTA (see the note at the top).
+constexpr uint32_t kGUSmemMin = (kSmemPerSM - 2 * kSmemReserved) / 2 + 16;
+constexpr uint32_t kGUSmemUsed = kGUMisc + 16 + 1024;   // + alignment slack of the base
+constexpr uint32_t kGUSmem = kGUSmemUsed > kGUSmemMin ? kGUSmemUsed : kGUSmemMin;
 // Shared memory of the down kernel: stages, kHRing h tiles, their group records, then
 // barriers full[S], empty[S], acc_full[B], acc_empty[B], h_full[R], h_empty[R], drain,
 // then the misc words.
 constexpr int kHRing = 4;
+constexpr int kGUMaxRegs = 64;
+constexpr int kDnMaxRegs = 192;
+static_assert(2 * 32 * (kGUMaxRegs + kDnMaxRegs) <= 16384, "two warps of each kernel per sub-partition");
 constexpr int kDnSub = 2;                     // f tiles per down item: blocks of one d block accumulate
 constexpr int kDnThreads = 256;               // + warps 6-7: the h formers
 constexpr uint32_t kDnH = kDownStages * kWBytes;
@@ -85,7 +94,8 @@ constexpr uint32_t kDnBars = kDnInfo + kHRing * kInfoBytes;
 constexpr uint32_t kDnNumBars = 2 * kDownStages + 2 * kDownBufs + 2 * kHRing + 1;
 constexpr uint32_t kDnMisc = kDnBars + 8 * kDnNumBars;
 constexpr uint32_t kDnSmem = kDnMisc + 16 + 1024;
-static_assert(kGUSmem + kDnSmem + 2048 <= 233472, "a gate/up and a down CTA must share one SM");
+static_assert(kGUSmem + kDnSmem + 2 * kSmemReserved <= kSmemPerSM, "a gate/up and a down CTA must share one SM");
+static_assert(2 * (kGUSmem + kSmemReserved) > kSmemPerSM, "two gate/up CTAs must not fit one SM");
 
 // Equal contiguous ranges of `blocks` work blocks over `parts` CTAs: CTA c takes
 // [lo(c), lo(c + 1)).
@@ -208,7 +218,7 @@ __device__ __forceinline__ void drain_copies(uint32_t bar_full, uint32_t cnt, in
 
 // ==================================================================== gate/up kernel
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(kGUMaxRegs)
 expert_gu_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
                  const __grid_constant__ CUtensorMap tm_x, const ExpertArgs a, float *const part,
                  const int zero_y) {
@@ -396,7 +406,10 @@ expert_gu_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
 
 // ==================================================================== down kernel
 
-__global__ void __launch_bounds__(kDnThreads, 1)
+// Registers: one SM sub-partition (a quarter of the 64K register file) holds up to two
+// warps of each kernel, so 2 * 32 * (down registers) + 2 * 32 * (gate/up registers) must stay
+// within 16384: with the gate/up kernel at 64, the down kernel gets at most 192.
+__global__ void __maxnreg__(kDnMaxRegs)
 expert_down_kernel(const __grid_constant__ CUtensorMap tm_wd, const ExpertArgs a, const float *const part,
                    const int gu_grid) {
     extern __shared__ uint8_t smem_raw[];
@@ -604,6 +617,9 @@ expert_down_kernel(const __grid_constant__ CUtensorMap tm_wd, const ExpertArgs a
                     while (ob <= u.ob_last() && u.s_lo(ob) >= u.s_hi(ob)) ++ob;   // no real sub-tile
                     if (ob > u.ob_last()) break;
                     const uint32_t buf = dcnt % kDownBufs, dph = (dcnt / kDownBufs) & 1u;
+                    // the first unit of a batch is waited for; later ones join only if
+                    // already complete, so a batch never holds back finished accumulators
+                    if (j > 0 && !__all_sync(kFull, mbar_try_wait(bar_acc_full + 8u * buf, dph))) break;
                     if (!warp_wait(bar_acc_full + 8u * buf, dph, abort_flag, a.err)) {
                         ok = false;
                         break;
