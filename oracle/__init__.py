@@ -63,6 +63,21 @@ def _load():
         lib.oracle_best_draft_length.argtypes = [P, I, D]
         lib.oracle_crossover.argtypes = [P, P, I, I]
         lib.oracle_bandwidth_report.argtypes = [I, I, P, P, P, P, P, P, P, P, P, P]
+        for name, args in (("oracle_throughput", [P, I, D]), ("oracle_first_threshold", [P]),
+                           ("oracle_speedup", [P, I, D]), ("oracle_alpha", [P, I, I]),
+                           ("oracle_convex_step_point", [P, I]), ("oracle_mean_reuse", [I, P, P, I, I]),
+                           ("oracle_reuse_threshold", [I, D, D, D, D, D, D, D]),
+                           ("oracle_reuse_threshold_bytes", [I, D, D, D, D]),
+                           ("oracle_err_verify_factor", [D]), ("oracle_err_saving_bound", [D, D, D]),
+                           ("oracle_err_regret_factor", [D])):
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = D
+        lib.oracle_step_points.argtypes = [P, I, P]
+        lib.oracle_convex_nondecreasing.argtypes = [P, I]
+        lib.oracle_err_decision_agrees.argtypes = [D, D, D]
+        lib.oracle_err_kstar_separated.argtypes = [P, I, D, D]
+        lib.oracle_err_speedup_interval.argtypes = [D, P, P]
         _lib = lib
     return _lib
 
@@ -229,3 +244,91 @@ def bandwidth_report(n_lo, slot_bytes, dedup_bytes, t_slot, t_dedup):
     res = dict(zip(("beta_slot", "beta_dedup", "ubar", "r", "saving"), outs))
     res["crossover"] = None if cross[0] < 0 else int(cross[0])
     return res
+
+
+# ---------------------------------------------------------------- step-time theory
+def _V(V):
+    return np.ascontiguousarray(V, dtype=np.float64)
+
+
+def throughput(V, k: int, a: float) -> float:
+    V = _V(V)
+    return float(_load().oracle_throughput(_ptr(V), int(k), float(a)))
+
+
+def first_threshold(V) -> float:
+    V = _V(V)
+    return float(_load().oracle_first_threshold(_ptr(V)))
+
+
+def speedup(V, k: int, a: float) -> float:
+    V = _V(V)
+    return float(_load().oracle_speedup(_ptr(V), int(k), float(a)))
+
+
+def alpha(V, k: int, i: int) -> float:
+    V = _V(V)
+    return float(_load().oracle_alpha(_ptr(V), int(k), int(i)))
+
+
+def step_points(V) -> np.ndarray:
+    """a_step[0..kmax], a_step[0] = 0 (B.31)."""
+    V = _V(V)
+    out = np.zeros(len(V), np.float64)
+    if _load().oracle_step_points(_ptr(V), len(V) - 1, _ptr(out)) != 0:
+        raise ValueError("oracle_step_points: kmax < 1 or a non-positive step time")
+    return out
+
+
+def convex_nondecreasing(V) -> bool:
+    V = _V(V)
+    return bool(_load().oracle_convex_nondecreasing(_ptr(V), len(V) - 1))
+
+
+def convex_step_point(V, j: int) -> float:
+    V = _V(V)
+    return float(_load().oracle_convex_step_point(_ptr(V), int(j)))
+
+
+def mean_reuse(w, rho, k: int) -> float:
+    """rho_bar_k of (11): w [L], rho [L, jmax+1]."""
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    rho = np.ascontiguousarray(rho, dtype=np.float64)
+    return float(_load().oracle_mean_reuse(len(w), _ptr(w), _ptr(rho), rho.shape[1] - 1, int(k)))
+
+
+def reuse_threshold(k, a, mW, Bk, beta1, tau1, dD_bD=0.0, dphi=0.0) -> float:
+    return float(_load().oracle_reuse_threshold(int(k), float(a), float(mW), float(Bk), float(beta1),
+                                                float(tau1), float(dD_bD), float(dphi)))
+
+
+def reuse_threshold_bytes(k, a, mW, D1=0.0, Dk1=0.0) -> float:
+    return float(_load().oracle_reuse_threshold_bytes(int(k), float(a), float(mW), float(D1), float(Dk1)))
+
+
+def err_verify_factor(eps) -> float:
+    return float(_load().oracle_err_verify_factor(float(eps)))
+
+
+def err_saving_bound(eps, Me_slot, Me_dedup) -> float:
+    return float(_load().oracle_err_saving_bound(float(eps), float(Me_slot), float(Me_dedup)))
+
+
+def err_decision_agrees(r, ubar, eps) -> bool:
+    return bool(_load().oracle_err_decision_agrees(float(r), float(ubar), float(eps)))
+
+
+def err_regret_factor(delta) -> float:
+    return float(_load().oracle_err_regret_factor(float(delta)))
+
+
+def err_kstar_separated(V, a, delta) -> bool:
+    V = _V(V)
+    return bool(_load().oracle_err_kstar_separated(_ptr(V), len(V) - 1, float(a), float(delta)))
+
+
+def err_speedup_interval(delta):
+    lo = np.zeros(1, np.float64)
+    hi = np.zeros(1, np.float64)
+    _load().oracle_err_speedup_interval(float(delta), _ptr(lo), _ptr(hi))
+    return float(lo[0]), float(hi[0])

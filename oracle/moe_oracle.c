@@ -25,6 +25,12 @@
  *   oracle_reuse_estimate    closed form of the synthetic trace law
  *   oracle_best_draft_length the pages' jump example, exact rational brute force
  *   oracle_crossover         hand cases of the definition
+ *   oracle_alpha / oracle_step_points / oracle_convex_step_point
+ *                            closed forms (k, i) = (1,0), (2,0), (2,1); polynomial roots;
+ *                            the brute-force staircase k*(a) on fine grids; the jump example
+ *   oracle_reuse_threshold*  the pages' counterexample (rho*_1 = 7/20, rho*_2 = 371/800 and
+ *                            its three patterns); identity (B.13); brute-force speedups
+ *   oracle_err_*             random perturbations of every bandwidth within the bound
  */
 #include <math.h>
 #include <stdint.h>
@@ -412,4 +418,216 @@ int oracle_bandwidth_report(int n_lo, int count, const double *slot_bytes,
     }
     *cross = oracle_crossover(t_slot, t_dedup, n_lo, n_lo + count - 1);
     return 0;
+}
+
+/* ------------------------------------------------------------------ step-time theory */
+
+/* T_a(k) = G_a(k) / V(k), the throughput of draft length k [Lan, §1 "Speculative decoding"]. */
+double oracle_throughput(const double *V, int k, double a)
+{
+    return oracle_expected_tokens(a, k) / V[k];
+}
+
+/*
+ * a0 = V(1)/V(0) - 1 [Lan, §3.2 and App. B.1 (B.4)]: one draft is faster than none exactly
+ * when a > a0.
+ */
+double oracle_first_threshold(const double *V)
+{
+    return V[1] / V[0] - 1.0;
+}
+
+/* The speedup T_a(k)/T_a(0) = G_a(k) V(0) / V(k) [Lan, §3.2 (9)]. */
+double oracle_speedup(const double *V, int k, double a)
+{
+    return oracle_throughput(V, k, a) / oracle_throughput(V, 0, a);
+}
+
+/*
+ * alpha_{k,i} [Lan, App. B.3]: the infimum of J_{k,i} = {a in [0,1) : T_a(k) > T_a(i)},
+ * taken as 1 when J_{k,i} is empty (0 <= i < k).  J_{k,i} is closed upward in [0,1)
+ * ((B.26)-(B.27)): G_a(k)/G_a(i) rises with a from 1 at a = 0 towards (k+1)/(i+1) as
+ * a -> 1.  So: if T_0(k) > T_0(i) the infimum is 0; if (k+1)/(i+1) <= V(k)/V(i) no a < 1
+ * qualifies and the value is 1; otherwise the boundary is found by halving an interval
+ * [lo, hi] with lo outside and hi inside J_{k,i}, testing T_a(k) > T_a(i) directly.
+ */
+/*
+ * T_a(k) > T_a(i) for i < k, multiplied through by V(k) V(i) > 0 and with G_a(k) split as
+ * G_a(i) + a^{i+1} + ... + a^k: V(i) (a^{i+1} + ... + a^k) > G_a(i) (V(k) - V(i)).  The
+ * same inequality, without the cancellation of comparing two nearly equal throughputs.
+ */
+static int oracle_faster(const double *V, int k, int i, double a)
+{
+    double tail = 0.0, p = 1.0;
+    for (int s = 0; s <= k; ++s) {
+        if (s > i) tail += p;
+        p *= a;
+    }
+    return V[i] * tail > oracle_expected_tokens(a, i) * (V[k] - V[i]) ? 1 : 0;
+}
+
+double oracle_alpha(const double *V, int k, int i)
+{
+    if (oracle_faster(V, k, i, 0.0)) return 0.0;
+    if ((double)(k + 1) * V[i] <= (double)(i + 1) * V[k]) return 1.0;
+    double lo = 0.0, hi = 1.0;
+    for (int it = 0; it < 200; ++it) {
+        double mid = 0.5 * (lo + hi);
+        if (mid <= lo || mid >= hi) break;
+        if (oracle_faster(V, k, i, mid)) hi = mid;
+        else lo = mid;
+    }
+    return hi;
+}
+
+/*
+ * Step points a_j = max over i < j of min over k >= j of alpha_{k,i}, j = 1..kmax
+ * [Lan, §3.3 and App. B.3 (B.31)]: k*(a) >= j for every a in (a_j, 1) and k*(a) < j for
+ * every a in [0, a_j).  a_step[0] = 0.  Returns 0, or -1 if kmax < 1 or some V <= 0.
+ */
+int oracle_step_points(const double *V, int kmax, double *a_step)
+{
+    if (kmax < 1) return -1;
+    for (int k = 0; k <= kmax; ++k)
+        if (!(V[k] > 0.0)) return -1;
+    a_step[0] = 0.0;
+    for (int j = 1; j <= kmax; ++j) {
+        double mx = 0.0;
+        for (int i = 0; i < j; ++i) {
+            double mn = 1.0;
+            for (int k = j; k <= kmax; ++k) {
+                double al = oracle_alpha(V, k, i);
+                if (al < mn) mn = al;
+            }
+            if (i == 0 || mn > mx) mx = mn;
+        }
+        a_step[j] = mx;
+    }
+    return 0;
+}
+
+/*
+ * Convex and non-decreasing step time [Lan, §3.3 (10)]: c_i = V(i) - V(i-1) with
+ * 0 <= c_1 <= c_2 <= ... <= c_kmax.  Returns 1 if so, else 0.
+ */
+int oracle_convex_nondecreasing(const double *V, int kmax)
+{
+    double prev = 0.0;
+    for (int i = 1; i <= kmax; ++i) {
+        double c = V[i] - V[i - 1];
+        if (c < prev) return 0;
+        prev = c;
+    }
+    return 1;
+}
+
+/*
+ * The step point a_j of a convex non-decreasing step time [Lan, App. B.3 (B.36)]:
+ * a_j = inf {a in [0,1) : h_j(a) > c_j / V(j-1)} with h_j(a) = a^j / G_a(j-1), strictly
+ * increasing on [0,1); a_1 = min(c_1/V(0), 1).  The infimum is found by halving, testing
+ * the defining inequality a^j V(j-1) > G_a(j-1) c_j of (10).  Returns 1 when the set is
+ * empty (h_j never exceeds the bound below a = 1).
+ */
+double oracle_convex_step_point(const double *V, int j)
+{
+    double c = V[j] - V[j - 1];
+    if (j == 1) {
+        double v = c / V[0];
+        return v < 1.0 ? v : 1.0;
+    }
+    /* at a = 0 the left side is 0 and never exceeds a non-negative right side */
+    double hi_lim = 1.0, lo = 0.0, hi = 1.0;
+    /* as a -> 1, a^j V(j-1) -> V(j-1) and G_a(j-1) c_j -> j c_j */
+    if (V[j - 1] <= (double)j * c) return hi_lim;
+    for (int it = 0; it < 200; ++it) {
+        double mid = 0.5 * (lo + hi);
+        if (mid <= lo || mid >= hi) break;
+        if (pow(mid, (double)j) * V[j - 1] > oracle_expected_tokens(mid, j - 1) * c) hi = mid;
+        else lo = mid;
+    }
+    return hi;
+}
+
+/*
+ * Byte-weighted mean reuse of the k drafted tokens [Lan, §3.4 (11)]:
+ * rho_bar_k = (1/(k W)) sum_{j=2}^{k+1} sum_l w_l rho_l(j), W = sum_l w_l.
+ * rho [L][jmax+1] row-major (rho[l][j] for j = 0..jmax), w [L].  Requires k+1 <= jmax.
+ */
+double oracle_mean_reuse(int L, const double *w, const double *rho, int jmax, int k)
+{
+    double W = 0.0, acc = 0.0;
+    for (int l = 0; l < L; ++l) W += w[l];
+    for (int j = 2; j <= k + 1; ++j)
+        for (int l = 0; l < L; ++l) acc += w[l] * rho[l * (jmax + 1) + j];
+    return acc / ((double)k * W);
+}
+
+/*
+ * Reuse threshold in time [Lan, §3.4 (14), App. B.2 (B.12)-(B.14)]:
+ *   rho*_k(a) = 1 - (1/k) [ B_k Y / (m W) + B_k / beta(1) - 1 ],
+ *   Y = (G_a(k) - 1) tau(1) - dD_k / beta_D - dphi_k,
+ * the bracket of (14) written out; a draft of length k is faster than plain decoding
+ * exactly when rho_bar_k > rho*_k(a).
+ *   mW = m W, Bk = beta_dedup(k+1), beta1 = beta(1), tau1 = tau(1),
+ *   dD_bD = (D(k+1) - D(1)) / beta_D, dphi = phi_dedup(k+1) - phi(1).
+ */
+double oracle_reuse_threshold(int k, double a, double mW, double Bk, double beta1, double tau1,
+                              double dD_bD, double dphi)
+{
+    double Y = (oracle_expected_tokens(a, k) - 1.0) * tau1 - dD_bD - dphi;
+    return 1.0 - (Bk * Y / mW + Bk / beta1 - 1.0) / (double)k;
+}
+
+/*
+ * Reuse threshold in bytes, one bandwidth and t0 = phi = 0 [Lan, §3.4 (16), (B.16)]:
+ *   rho*_k(a) = 1 - [ (G_a(k) - 1)(D(1) + m W) - (D(k+1) - D(1)) ] / (m W k).
+ */
+double oracle_reuse_threshold_bytes(int k, double a, double mW, double D1, double Dk1)
+{
+    return 1.0 - ((oracle_expected_tokens(a, k) - 1.0) * (D1 + mW) - (Dk1 - D1)) / (mW * (double)k);
+}
+
+/*
+ * Error bounds [Lan, §3.5, Table 2, App. C], for a relative bandwidth error |e| <= eps < 1
+ * (each bandwidth estimated as beta (1 + e)), and delta = eps / (1 - eps) for the step time.
+ */
+/* (17): |tau_hat - tau| <= eps/(1-eps) M_p(n); returns the factor eps/(1-eps). */
+double oracle_err_verify_factor(double eps) { return eps / (1.0 - eps); }
+
+/* (18): |S_hat - S| <= eps/(1-eps) (M^e_slot + M^e_dedup). */
+double oracle_err_saving_bound(double eps, double Me_slot, double Me_dedup)
+{
+    return eps / (1.0 - eps) * (Me_slot + Me_dedup);
+}
+
+/* (19): the predicted and the true faster kernel agree if |ln r - ln u_bar| > ln((1+eps)/(1-eps)). */
+int oracle_err_decision_agrees(double r, double ubar, double eps)
+{
+    return fabs(log(r) - log(ubar)) > log((1.0 + eps) / (1.0 - eps)) ? 1 : 0;
+}
+
+/* (20): T_a(k_hat*) >= (1-delta)/(1+delta) T_a(k*); returns (1-delta)/(1+delta). */
+double oracle_err_regret_factor(double delta) { return (1.0 - delta) / (1.0 + delta); }
+
+/*
+ * (20) separation: k_hat* = k* if (1+delta)/(1-delta) T_a(i) < T_a(k*) for every i != k*.
+ * Returns 1 if the separation holds for step time V at acceptance a, else 0.
+ */
+int oracle_err_kstar_separated(const double *V, int kmax, double a, double delta)
+{
+    int ks = oracle_best_draft_length(V, kmax, a);
+    if (ks < 0) return 0;
+    double Tk = oracle_throughput(V, ks, a);
+    for (int i = 0; i <= kmax; ++i) {
+        if (i == ks) continue;
+        if (!((1.0 + delta) / (1.0 - delta) * oracle_throughput(V, i, a) < Tk)) return 0;
+    }
+    return 1;
+}
+
+/* (21): the best predicted speedup lies in [(1-delta)/(1+delta), (1+delta)/(1-delta)] times the true one. */
+void oracle_err_speedup_interval(double delta, double *lo, double *hi)
+{
+    *lo = (1.0 - delta) / (1.0 + delta);
+    *hi = (1.0 + delta) / (1.0 - delta);
 }
