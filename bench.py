@@ -149,6 +149,42 @@ def barrier(world: int):
         dist.barrier()
 
 
+def step_time_theory(n_values, Vs, Vd, Vw, bytes_slot, bytes_dedup, K):
+    """The step-time theory of the pages on the measured expert times (all 48 layers):
+    a0, the step points and the convexity test for each engine; for the deduplicating one,
+    the mean reuse of the drafted tokens from the union bytes (12) and the reuse threshold in
+    time (14) from the measured bandwidths, with the speedup decision (B.14) beside the one
+    the step times give directly; and the error bounds at a 10% bandwidth error."""
+    out = {}
+    for name, V in (("slot", Vs), ("dedup", Vd), ("switched", Vw)):
+        st = api.staircase(V)
+        out[name] = dict(a0=round(st["a0"], 6), a_step=[round(float(x), 6) for x in st["a_step"]],
+                         convex=st["convex"])
+    # dedup engine: one-token pass on the per-slot kernel (tau(1) = V(0)), B_k = beta_dedup(k+1)
+    mW = bytes_dedup[n_values[0]] / K
+    tau1 = Vd[0]
+    beta1 = mW / tau1
+    kmax = len(n_values) - 1
+    rho_bar, B = [], []
+    for k in range(1, kmax + 1):
+        E = bytes_dedup[n_values[k]] / K
+        rho_bar.append(1.0 - (E - mW) / (mW * k))
+        B.append(E / Vd[k])
+    decisions = {}
+    agree = True
+    for a in A_GRID:
+        thr = [api.reuse_threshold(k, a, mW, B[k - 1], beta1, tau1) for k in range(1, kmax + 1)]
+        by_reuse = any(rb > t for rb, t in zip(rho_bar, thr))
+        by_time = api.best_draft_length(Vd, a) >= 1
+        agree = agree and (by_reuse == by_time)
+        decisions[str(a)] = dict(speedup=by_reuse, rho_star=[round(t, 5) for t in thr[:4]])
+    out["dedup_reuse"] = dict(rho_bar=[round(x, 5) for x in rho_bar], decisions=decisions,
+                              agrees_with_step_times=agree)
+    eb = api.error_bounds(0.10)
+    out["error_bounds_eps_0.10"] = {k: round(v, 6) for k, v in eb.items()}
+    return out
+
+
 def kernel_traffic(kernel: str):
     """DRAM bytes per launch of a kernel from the committed ncu summary, when it was taken on
     the current source of that kernel; None otherwise."""
@@ -367,6 +403,9 @@ def run_ours(args, world, rank, local):
         for a in A_GRID:
             kstar[str(a)] = dict(slot=api.best_draft_length(Vs, a), dedup=api.best_draft_length(Vd, a),
                                  switched=api.best_draft_length(Vw, a))
+        theory = step_time_theory(n_values, Vs, Vd, Vw, bytes_slot, bytes_dedup, K)
+    else:
+        theory = None
 
     # roofline of the expert op (both forms; one launch = one layer's expert op, the
     # gate/up and down kernels chained by programmatic dependent launch, which overlap:
@@ -392,7 +431,7 @@ def run_ours(args, world, rank, local):
                             l2="inputs larger than L2: 57.98 GB of weights streamed layer after layer"
                             if layers == 48 else f"{layers} layers, no flush"),
                 roofline=roofline, gpu_launches=b.launches_per_step * K,
-                clocks=clk.summary(), per_n=per_n, crossover=rep["crossover"], kstar=kstar,
+                clocks=clk.summary(), per_n=per_n, crossover=rep["crossover"], kstar=kstar, theory=theory,
                 self_check=dict(max_slot_vs_dedup_rel=round(self_check, 6), device_error=err),
                 setup_s=dict(weights=round(b.t_weights, 1)))
 

@@ -247,6 +247,84 @@ double moe_expected_union(int32_t N, int32_t m, int32_t n);
 int32_t moe_best_draft_length(const double *V, int32_t kmax, double a);
 
 /*
+ * Staircase of a step time [Lan, §3.2 (8)-(9) and App. B.1 (B.4): a0 = V(1)/V(0) - 1 is the
+ * acceptance above which one draft beats none; §3.3 and App. B.3 (B.26)-(B.31): alpha_{k,i}
+ * = inf {a in [0,1) : T_a(k) > T_a(i)} (1 if empty) and the step points
+ * a_j = max_{i<j} min_{k>=j} alpha_{k,i}, so that k*(a) >= j for a in (a_j, 1) and k*(a) < j
+ * for a in [0, a_j); (10): with 0 <= c_1 <= ... <= c_kmax, c_i = V(i) - V(i-1), j - 1 and j
+ * alone decide whether k*(a) reaches j].  Host only.
+ *   V      [host] double [kmax+1], the step time of a step drafting k tokens, all > 0;
+ *          1 <= kmax <= 64.
+ *   a0     out: V(1)/V(0) - 1 (may be negative, or >= 1).
+ *   a_step [host] double [kmax+1] out: a_step[0] = 0, a_step[j] the j-th step point.
+ *   alpha  [host] double [(kmax+1)*(kmax+1)] out, or NULL: alpha[k*(kmax+1) + i] for i < k,
+ *          0 elsewhere.
+ *   convex out: 1 if V is convex and non-decreasing (the hypothesis of (10)), else 0.
+ * Returns MOE_ERR_ARG for a NULL output, kmax outside [1, 64] or a V <= 0 or not finite.
+ */
+moe_status_t moe_staircase(const double *V, int32_t kmax, double *a0, double *a_step, double *alpha,
+                           int32_t *convex);
+
+/*
+ * Speedup of draft length k over plain decoding [Lan, §3.2 (9)]:
+ * T_a(k)/T_a(0) = G_a(k) V(0) / V(k).  Host only; NAN for k outside [0, kmax], a outside
+ * [0, 1) or a V <= 0.
+ */
+double moe_speedup(const double *V, int32_t kmax, int32_t k, double a);
+
+/*
+ * Reuse threshold of a deduplicating engine in time [Lan, §3.4 (14), App. B.2 (B.12)-(B.14)]:
+ * a draft of length k is faster than plain decoding exactly when the byte-weighted mean reuse
+ * rho_bar_k of the k drafted tokens (11) exceeds
+ *   rho*_k(a) = 1 - (B_k / (m W k)) [ (G_a(k) - 1) tau(1) - dD_k / beta_D - dphi_k ]
+ *                 - (B_k / beta(1) - 1) / k.
+ * Host only.  in: mW = m W (expert bytes of a one-token pass), B_k = beta_dedup(k+1),
+ * beta_1 = beta(1), tau_1 = tau(1) = V(0), dD_over_betaD = (D(k+1) - D(1)) / beta_D,
+ * dphi = phi_dedup(k+1) - phi(1) (any consistent units).  NAN for k < 1, a outside [0, 1),
+ * or mW, B_k, beta_1 not > 0.
+ */
+typedef struct {
+    double mW, B_k, beta_1, tau_1, dD_over_betaD, dphi;
+} moe_threshold_in_t;
+
+double moe_reuse_threshold(int32_t k, double a, const moe_threshold_in_t *in);
+
+/*
+ * The same threshold with one bandwidth and no fixed time [Lan, §3.4 (16), (B.16)]:
+ *   rho*_k(a) = 1 - [ (G_a(k) - 1)(D(1) + m W) - (D(k+1) - D(1)) ] / (m W k),
+ * D(n) = D + kv(n-1) the bytes read once per pass.  Host only; NAN for k < 1, a outside
+ * [0, 1) or mW not > 0.
+ */
+double moe_reuse_threshold_bytes(int32_t k, double a, double mW, double D_1, double D_k1);
+
+/*
+ * Error bounds for a relative bandwidth error |e| <= eps < 1/2 [Lan, §3.5, Table 2, App. C]:
+ *   delta         = eps / (1 - eps), the relative error of a predicted step time;
+ *   verify_factor = eps / (1 - eps): |tau_hat - tau| <= verify_factor * M_p(n) (17), and
+ *                   |S_hat - S| <= verify_factor * (M^e_slot + M^e_dedup) (18);
+ *   decision_log_margin = ln((1+eps)/(1-eps)): the predicted and true faster kernel agree
+ *                   when |ln r(n) - ln u_bar(n)| exceeds it (19);
+ *   regret_factor = (1-delta)/(1+delta): T_a(k_hat*) >= regret_factor * T_a(k*) (20);
+ *   speedup_lo, speedup_hi = (1-delta)/(1+delta), (1+delta)/(1-delta): the best predicted
+ *                   speedup over the true one (21) ((1+delta)/(1-delta) = 1/(1-2 eps), (C.7)).
+ * Host only.  Returns MOE_ERR_ARG for eps outside [0, 1/2) or a NULL out.
+ */
+typedef struct {
+    double delta, verify_factor, decision_log_margin, regret_factor, speedup_lo, speedup_hi;
+} moe_error_bounds_t;
+
+moe_status_t moe_error_bounds(double eps, moe_error_bounds_t *out);
+
+/*
+ * The separation condition of (20) [Lan, §3.5, Table 2]: with step-time errors within
+ * delta, the predicted best draft length equals the true one when
+ * (1+delta)/(1-delta) T_a(i) < T_a(k*) for every i != k*.  Host only.  Returns 1 if it holds
+ * for V at acceptance a, 0 if not, -1 for bad arguments (as moe_best_draft_length, or
+ * delta outside [0, 1)).
+ */
+int32_t moe_kstar_separated(const double *V, int32_t kmax, double a, double delta);
+
+/*
  * Synchronises stream s, reads the device error word of the workspace [dev] into *code
  * (a moe_status_t value; MOE_OK if nothing was recorded) and clears it.
  */

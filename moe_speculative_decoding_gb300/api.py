@@ -46,10 +46,21 @@ class _PassBytes(ctypes.Structure):
                 ("reserved", ctypes.c_int32), ("ubar", ctypes.c_double)]
 
 
+class ThresholdIn(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_double) for f in ("mW", "B_k", "beta_1", "tau_1", "dD_over_betaD", "dphi")]
+
+
+class _ErrorBounds(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_double) for f in ("delta", "verify_factor", "decision_log_margin", "regret_factor",
+                                               "speedup_lo", "speedup_hi")]
+
+
 EXPORTED = ("moe_abi_version", "moe_status_str", "moe_workspace_bytes", "moe_workspace_init",
             "moe_route_topm", "moe_group_slots", "moe_expert_op_perslot", "moe_expert_op_dedup",
             "moe_pass_bytes", "moe_bandwidth_report", "moe_expected_union",
-            "moe_best_draft_length", "moe_last_device_error", "moe_expert_op_perslot_noalloc")
+            "moe_best_draft_length", "moe_last_device_error", "moe_expert_op_perslot_noalloc",
+            "moe_staircase", "moe_speedup", "moe_reuse_threshold", "moe_reuse_threshold_bytes",
+            "moe_error_bounds", "moe_kstar_separated")
 
 _lib = None
 
@@ -84,6 +95,12 @@ def lib():
         "moe_expected_union": ([I32, I32, I32], D),
         "moe_best_draft_length": ([P, I32, D], I32),
         "moe_last_device_error": ([P, P, P], I32),
+        "moe_staircase": ([P, I32, P, P, P, P], I32),
+        "moe_speedup": ([P, I32, I32, D], D),
+        "moe_reuse_threshold": ([I32, D, ctypes.POINTER(ThresholdIn)], D),
+        "moe_reuse_threshold_bytes": ([I32, D, D, D, D], D),
+        "moe_error_bounds": ([D, ctypes.POINTER(_ErrorBounds)], I32),
+        "moe_kstar_separated": ([P, I32, D, D], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -259,3 +276,51 @@ def best_draft_length(V, a: float) -> int:
     if k < 0:
         raise MoeError(1, "moe_best_draft_length")
     return k
+
+
+# ---------------------------------------------------------------- step-time theory
+def _times(V) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(V, dtype=np.float64))
+
+
+def staircase(V) -> dict:
+    """a0, the step points a_step[0..kmax] (a_step[0] = 0), alpha[k, i] and the convex flag."""
+    V = _times(V)
+    K = V.size
+    a0 = ctypes.c_double(0.0)
+    steps = np.zeros(K, np.float64)
+    alpha = np.zeros((K, K), np.float64)
+    convex = ctypes.c_int32(0)
+    _check(lib().moe_staircase(ctypes.c_void_p(V.ctypes.data), K - 1, ctypes.byref(a0),
+                               ctypes.c_void_p(steps.ctypes.data), ctypes.c_void_p(alpha.ctypes.data),
+                               ctypes.byref(convex)), "moe_staircase")
+    return dict(a0=a0.value, a_step=steps, alpha=alpha, convex=bool(convex.value))
+
+
+def speedup(V, k: int, a: float) -> float:
+    V = _times(V)
+    return float(lib().moe_speedup(ctypes.c_void_p(V.ctypes.data), V.size - 1, int(k), float(a)))
+
+
+def reuse_threshold(k: int, a: float, mW: float, B_k: float, beta_1: float, tau_1: float,
+                    dD_over_betaD: float = 0.0, dphi: float = 0.0) -> float:
+    t = ThresholdIn(mW, B_k, beta_1, tau_1, dD_over_betaD, dphi)
+    return float(lib().moe_reuse_threshold(int(k), float(a), ctypes.byref(t)))
+
+
+def reuse_threshold_bytes(k: int, a: float, mW: float, D_1: float = 0.0, D_k1: float = 0.0) -> float:
+    return float(lib().moe_reuse_threshold_bytes(int(k), float(a), float(mW), float(D_1), float(D_k1)))
+
+
+def error_bounds(eps: float) -> dict:
+    out = _ErrorBounds()
+    _check(lib().moe_error_bounds(float(eps), ctypes.byref(out)), "moe_error_bounds")
+    return {f: getattr(out, f) for f, _ in _ErrorBounds._fields_}
+
+
+def kstar_separated(V, a: float, delta: float) -> bool:
+    V = _times(V)
+    r = int(lib().moe_kstar_separated(ctypes.c_void_p(V.ctypes.data), V.size - 1, float(a), float(delta)))
+    if r < 0:
+        raise MoeError(1, "moe_kstar_separated")
+    return bool(r)

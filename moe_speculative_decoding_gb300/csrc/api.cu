@@ -5,6 +5,7 @@
 // "Bytes"), effective bandwidth, u_bar and r (§2), the saving and the crossover (§3.1,
 // §2 "Testing the inputs"), E[U] under uniform routing (§1) and the best draft length
 // (§1 "Speculative decoding").
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <vector>
@@ -270,6 +271,130 @@ int32_t moe_best_draft_length(const double *V, int32_t kmax, double a) {
         }
     }
     return best;
+}
+
+// ---------------------------------------------------------------- step-time theory
+
+namespace {
+
+// G_a(k) = 1 + a + ... + a^k by Horner's rule.
+double expected_tokens(double a, int k) {
+    double g = 1.0;
+    for (int i = 0; i < k; ++i) g = 1.0 + a * g;
+    return g;
+}
+
+// q(a) > 0 exactly when T_a(k) > T_a(i) (i < k): G_a(k) V(i) - G_a(i) V(k), written as
+// V(i) a^{i+1} G_a(k-i-1) - G_a(i) (V(k) - V(i)) so that equal step times do not cancel.
+double faster_margin(const double *V, int k, int i, double a) {
+    return V[i] * std::pow(a, i + 1) * expected_tokens(a, k - i - 1) - expected_tokens(a, i) * (V[k] - V[i]);
+}
+
+// alpha_{k,i}: the boundary of {a in [0,1) : q(a) > 0}, an upward-closed set (G_a(k)/G_a(i)
+// rises with a towards (k+1)/(i+1)); bracketed regula falsi with the Illinois step.
+double alpha_of(const double *V, int k, int i) {
+    if (V[k] < V[i]) return 0.0;                                          // q(0) = V(i) - V(k)
+    if ((k + 1) * V[i] <= (i + 1) * V[k]) return 1.0;                     // q(a) <= 0 below a = 1
+    double lo = 0.0, hi = 1.0, qlo = faster_margin(V, k, i, 0.0), qhi = (k + 1) * V[i] - (i + 1) * V[k];
+    int side = 0;
+    for (int it = 0; it < 400 && hi - lo > 1e-17; ++it) {
+        double x = (qhi - qlo) != 0.0 ? (lo * qhi - hi * qlo) / (qhi - qlo) : 0.5 * (lo + hi);
+        if (!(x > lo && x < hi)) x = 0.5 * (lo + hi);
+        const double qx = faster_margin(V, k, i, x);
+        if (qx > 0.0) {
+            hi = x;
+            qhi = qx;
+            if (side == 1) qlo *= 0.5;
+            side = 1;
+        } else {
+            lo = x;
+            qlo = qx;
+            if (side == -1) qhi *= 0.5;
+            side = -1;
+        }
+    }
+    return hi;
+}
+
+bool valid_times(const double *V, int kmax) {
+    if (V == nullptr || kmax < 0) return false;
+    for (int k = 0; k <= kmax; ++k)
+        if (!(V[k] > 0.0) || !std::isfinite(V[k])) return false;
+    return true;
+}
+
+}  // namespace
+
+moe_status_t moe_staircase(const double *V, int32_t kmax, double *a0, double *a_step, double *alpha,
+                           int32_t *convex) {
+    if (kmax < 1 || kmax > 64 || !valid_times(V, kmax) || a0 == nullptr || a_step == nullptr || convex == nullptr)
+        return MOE_ERR_ARG;
+    const int K = kmax + 1;
+    std::vector<double> al(static_cast<size_t>(K) * K, 0.0);
+    for (int k = 1; k <= kmax; ++k)
+        for (int i = 0; i < k; ++i) al[static_cast<size_t>(k) * K + i] = alpha_of(V, k, i);
+    a_step[0] = 0.0;
+    for (int j = 1; j <= kmax; ++j) {
+        double best = 0.0;
+        for (int i = 0; i < j; ++i) {
+            double mn = 1.0;
+            for (int k = j; k <= kmax; ++k) mn = std::min(mn, al[static_cast<size_t>(k) * K + i]);
+            best = i == 0 ? mn : std::max(best, mn);
+        }
+        a_step[j] = best;
+    }
+    if (alpha != nullptr) std::memcpy(alpha, al.data(), al.size() * sizeof(double));
+    *a0 = V[1] / V[0] - 1.0;
+    int cv = 1;
+    double c_prev = 0.0;
+    for (int i = 1; i <= kmax; ++i) {
+        const double c = V[i] - V[i - 1];
+        if (c < c_prev) cv = 0;
+        c_prev = c;
+    }
+    *convex = cv;
+    return MOE_OK;
+}
+
+double moe_speedup(const double *V, int32_t kmax, int32_t k, double a) {
+    if (!valid_times(V, kmax) || k < 0 || k > kmax || !(a >= 0.0) || !(a < 1.0)) return NAN;
+    return expected_tokens(a, k) * V[0] / V[k];
+}
+
+double moe_reuse_threshold(int32_t k, double a, const moe_threshold_in_t *in) {
+    if (in == nullptr || k < 1 || !(a >= 0.0) || !(a < 1.0) || !(in->mW > 0.0) || !(in->B_k > 0.0) ||
+        !(in->beta_1 > 0.0))
+        return NAN;
+    const double bracket = (expected_tokens(a, k) - 1.0) * in->tau_1 - in->dD_over_betaD - in->dphi;
+    return 1.0 - in->B_k / (in->mW * k) * bracket - (in->B_k / in->beta_1 - 1.0) / k;
+}
+
+double moe_reuse_threshold_bytes(int32_t k, double a, double mW, double D_1, double D_k1) {
+    if (k < 1 || !(a >= 0.0) || !(a < 1.0) || !(mW > 0.0)) return NAN;
+    return 1.0 - ((expected_tokens(a, k) - 1.0) * (D_1 + mW) - (D_k1 - D_1)) / (mW * k);
+}
+
+moe_status_t moe_error_bounds(double eps, moe_error_bounds_t *out) {
+    if (out == nullptr || !(eps >= 0.0) || !(eps < 0.5)) return MOE_ERR_ARG;
+    const double d = eps / (1.0 - eps);
+    out->delta = d;
+    out->verify_factor = d;
+    out->decision_log_margin = std::log1p(eps) - std::log1p(-eps);
+    out->regret_factor = (1.0 - d) / (1.0 + d);
+    out->speedup_lo = (1.0 - d) / (1.0 + d);
+    out->speedup_hi = (1.0 + d) / (1.0 - d);
+    return MOE_OK;
+}
+
+int32_t moe_kstar_separated(const double *V, int32_t kmax, double a, double delta) {
+    if (!(delta >= 0.0) || !(delta < 1.0)) return -1;
+    const int32_t ks = moe_best_draft_length(V, kmax, a);
+    if (ks < 0) return -1;
+    const double top = expected_tokens(a, ks) / V[ks];
+    const double f = (1.0 + delta) / (1.0 - delta);
+    for (int32_t i = 0; i <= kmax; ++i)
+        if (i != ks && !(f * expected_tokens(a, i) / V[i] < top)) return 0;
+    return 1;
 }
 
 moe_status_t moe_last_device_error(void *ws, moe_stream_t s, int32_t *code) {

@@ -144,3 +144,75 @@ def test_expected_union_and_best_draft_length_match_oracle(lib, oracle_mod):
         assert api.best_draft_length(V, a) == oracle_mod.best_draft_length(V, a)
     with pytest.raises(api.MoeError):
         api.best_draft_length([1.0, -1.0], 0.5)
+
+
+# ------------------------------------------------------------------ step-time theory (host)
+
+def _rand_V(rng, kmax):
+    if rng.random() < 0.5:
+        c = np.sort(rng.uniform(0.0, 1.0, kmax))
+        v0 = rng.uniform(0.5, 2.0)
+        return np.concatenate([[v0], v0 + np.cumsum(c)])
+    return rng.uniform(0.2, 3.0, kmax + 1)
+
+
+def test_staircase_matches_oracle(lib, oracle_mod):
+    rng = np.random.default_rng(60)
+    for _ in range(300):
+        kmax = int(rng.integers(1, 9))
+        V = _rand_V(rng, kmax)
+        got = api.staircase(V)
+        assert np.allclose(got["a_step"], oracle_mod.step_points(V), rtol=0, atol=1e-12)
+        for k in range(1, kmax + 1):
+            for i in range(k):
+                assert abs(got["alpha"][k, i] - oracle_mod.alpha(V, k, i)) <= 1e-12
+        assert got["a0"] == oracle_mod.first_threshold(V)
+        assert got["convex"] == oracle_mod.convex_nondecreasing(V)
+        for a in rng.uniform(0, 1, 3):
+            for k in range(kmax + 1):
+                assert api.speedup(V, k, a) == pytest.approx(oracle_mod.speedup(V, k, a), rel=1e-14)
+    g = load_golden("staircase_jump.json")
+    st = api.staircase(g["V"])
+    assert st["a_step"][1] == pytest.approx((5 ** 0.5 - 1) / 2, abs=1e-14) and st["alpha"][1, 0] == 1.0
+
+
+def test_reuse_thresholds_match_oracle(lib, oracle_mod):
+    rng = np.random.default_rng(61)
+    for _ in range(300):
+        k, a = int(rng.integers(1, 9)), float(rng.uniform(0, 1))
+        args = [float(x) for x in (rng.uniform(1, 10), rng.uniform(0.3, 3), rng.uniform(0.3, 3), rng.uniform(1, 20),
+                                   rng.uniform(0, 2), rng.uniform(-1, 1))]
+        assert api.reuse_threshold(k, a, *args) == pytest.approx(oracle_mod.reuse_threshold(k, a, *args), rel=1e-13, abs=1e-13)
+        mW, D1 = float(rng.uniform(1, 10)), float(rng.uniform(0, 5))
+        Dk1 = D1 + float(rng.uniform(0, 3))
+        assert api.reuse_threshold_bytes(k, a, mW, D1, Dk1) == pytest.approx(
+            oracle_mod.reuse_threshold_bytes(k, a, mW, D1, Dk1), rel=1e-13, abs=1e-13)
+    g = load_golden("no_single_threshold.json")
+    a = g["a"][0] / g["a"][1]
+    for k, (p, q) in zip((1, 2), g["rho_star"]):
+        assert api.reuse_threshold_bytes(k, a, 1.0) == pytest.approx(p / q, abs=1e-15)
+    assert np.isnan(api.reuse_threshold_bytes(0, a, 1.0)) and np.isnan(api.reuse_threshold(1, 1.0, 1, 1, 1, 1))
+
+
+def test_error_bounds_and_separation_match_oracle(lib, oracle_mod):
+    rng = np.random.default_rng(62)
+    for eps in (0.0, 0.05, 0.1, 0.3, 0.49):
+        b = api.error_bounds(eps)
+        d = oracle_mod.err_verify_factor(eps)
+        assert b["delta"] == pytest.approx(d, rel=1e-15) and b["verify_factor"] == pytest.approx(d, rel=1e-15)
+        assert b["regret_factor"] == pytest.approx(oracle_mod.err_regret_factor(d), rel=1e-14)
+        lo, hi = oracle_mod.err_speedup_interval(d)
+        assert b["speedup_lo"] == pytest.approx(lo, rel=1e-14) and b["speedup_hi"] == pytest.approx(hi, rel=1e-14)
+        for _ in range(20):
+            r, u = float(rng.uniform(0.2, 1.5)), float(rng.uniform(0.2, 1.0))
+            assert (abs(np.log(r) - np.log(u)) > b["decision_log_margin"]) == oracle_mod.err_decision_agrees(r, u, eps)
+    for _ in range(200):
+        V = _rand_V(rng, int(rng.integers(1, 8)))
+        a, delta = float(rng.uniform(0, 1)), float(rng.uniform(0, 0.3))
+        assert api.kstar_separated(V, a, delta) == oracle_mod.err_kstar_separated(V, a, delta)
+    with pytest.raises(api.MoeError):
+        api.error_bounds(0.5)
+    with pytest.raises(api.MoeError):
+        api.staircase([1.0])
+    with pytest.raises(api.MoeError):
+        api.staircase([1.0, -2.0])
