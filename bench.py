@@ -62,6 +62,10 @@ def parse():
     p.add_argument("--n-max", type=int, default=None)
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-fit", action="store_true", help="skip the chosen-id fits (4) and (E.1)")
+    p.add_argument("--fit-only", action="store_true",
+                   help="only the chosen-id fits, on one freshly generated layer (prints their JSON)")
+    p.add_argument("--fit-reps", type=int, default=7)
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
 
@@ -183,6 +187,71 @@ def step_time_theory(n_values, Vs, Vd, Vw, bytes_slot, bytes_dedup, K):
     eb = api.error_bounds(0.10)
     out["error_bounds_eps_0.10"] = {k: round(v, 6) for k, v in eb.items()}
     return out
+
+
+def fit_leg(wl, weights, device, reps: int = 7, windows: int = 8, n_max: int = 16):
+    """Fits (4) and (E.1) of one layer's expert-operation time on passes with chosen ids, and
+    their error on windows of the layer's synthetic routing trace, the bandwidth error eps
+    ([Lan] §2 "Effective bandwidth", §4, App. E "Deduplicating fit").  Every pass follows a
+    write of 512 MiB (four times L2), so no pass finds its weights in L2."""
+    layer = api.make_layer(wl.d, wl.f, wl.N, wl.m, "bf16")
+    ws = api.workspace(layer, 16, device)
+    m, N = wl.m, wl.N
+    b = 3.0 * wl.d * wl.f * 2
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    x_all = synth.activations(n_max, wl.d, torch.bfloat16, synth.seed_for(wl.index, stream=77), device=device)
+    y = torch.empty((n_max, wl.d), dtype=torch.float32, device=device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def timed(n, ids_h):
+        ids = torch.from_numpy(np.ascontiguousarray(ids_h)).to(device)
+        gates = torch.full((n, m), 1.0 / m, dtype=torch.float32, device=device)
+        x = x_all[:n]
+        grp = api.Grouping.empty(n, m, N, device)
+        ts, td = [], []
+        for _ in range(reps):
+            flush.fill_(1)
+            ev[0].record()
+            api.expert_op_perslot(layer, weights, x, ids, gates, y=y[:n], ws=ws)
+            ev[1].record()
+            torch.cuda.synchronize(device)
+            ts.append(ev[0].elapsed_time(ev[1]) * 1e-3)
+            flush.fill_(2)
+            ev[0].record()
+            api.group_slots(ids, N, out=grp, ws=ws)
+            api.expert_op_dedup(layer, weights, x, gates, grp, y=y[:n], ws=ws)
+            ev[1].record()
+            torch.cuda.synchronize(device)
+            td.append(ev[0].elapsed_time(ev[1]) * 1e-3)
+        return float(np.median(ts)), float(np.median(td))
+
+    ns, Us, tss, tds = [], [], [], []
+    for n in range(2, n_max + 1):
+        hi = min(N, n * m)
+        for U in sorted(set(int(round(u)) for u in np.linspace(m, hi, 5))):
+            t_s, t_d = timed(n, synth.chosen_ids(n, m, N, U, seed=synth.seed_for(wl.index, stream=3000 + 131 * n + U)))
+            ns.append(n), Us.append(U), tss.append(t_s), tds.append(t_d)
+    slot = api.fit_op_times(ns, Us, tss, m, b, "slot")
+    dedup = api.fit_op_times(ns, Us, tds, m, b, "dedup")
+    # score on windows of the synthetic trace (the stand-in for recorded routing)
+    sets, _ = synth.routing_traces(1, windows * n_max, N, m, wl.rhos[0], seed=synth.seed_for(wl.index, stream=4000))
+    err_s, err_d = [], []
+    for n in range(2, n_max + 1):
+        for w in range(windows):
+            ids_h = sets[0, w * n:(w + 1) * n]
+            U = api.pass_bytes(layer, ids_h)["U"]
+            t_s, t_d = timed(n, ids_h)
+            err_s.append(abs(slot[0] + slot[1] * U * b + slot[2] * (n * m - U) * b - t_s) / t_s)
+            err_d.append(abs(dedup[0] + dedup[1] * U * b + dedup[2] * n - t_d) / t_d)
+    eps_s, eps_d = float(np.median(err_s)), float(np.median(err_d))
+    return dict(passes=len(ns), n_values=f"2..{n_max}", reps=reps, flush_bytes=512 << 20, b=int(b),
+                slot=dict(t_op_us=round(slot[0] * 1e6, 3), c_u_ps_per_byte=round(slot[1] * 1e12, 5),
+                          c_re_ps_per_byte=round(slot[2] * 1e12, 5), re_read_cost=round(slot[2] / slot[1], 4),
+                          first_read_tbps=round(1e-12 / slot[1], 3)),
+                dedup=dict(t_op_us=round(dedup[0] * 1e6, 3), c_g_ps_per_byte=round(dedup[1] * 1e12, 5),
+                           c_t_us_per_token=round(dedup[2] * 1e6, 4), union_tbps=round(1e-12 / dedup[1], 3)),
+                eps_slot=round(eps_s, 4), eps_dedup=round(eps_d, 4), eps=round(max(eps_s, eps_d), 4),
+                scored_windows=len(err_s))
 
 
 def kernel_traffic(kernel: str):
@@ -437,6 +506,8 @@ def run_ours(args, world, rank, local):
 
     if not args.no_e2e:
         line["e2e"] = e2e_run(b, args, world, device, total_bytes_per_step=total_bytes / K)
+    if rank == 0 and not args.no_fit:
+        line["fits"] = fit_leg(wl, b.weights[0], device, reps=args.fit_reps)
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(b)
     if rank == 0:
@@ -561,6 +632,13 @@ def main():
         # the oracle needs no collective: rank 0 runs it, other ranks exit without work
         world = int(os.environ.get("WORLD_SIZE", "1"))
         run_reference(args, world, int(os.environ.get("RANK", "0")))
+        return
+    if args.fit_only:
+        mbuild.build()
+        wl = BY_NAME[args.workload]
+        device = torch.device("cuda", 0)
+        w = synth.expert_weights(wl.N, wl.f, wl.d, torch.bfloat16, synth.seed_for(wl.index, layer=0), device=device)
+        print(json.dumps(dict(workload=wl.name, fits=fit_leg(wl, w, device, reps=args.fit_reps))), flush=True)
         return
     world, rank, local = dist_setup(args)
     run_ours(args, world, rank, local)

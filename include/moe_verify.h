@@ -325,6 +325,23 @@ moe_status_t moe_error_bounds(double eps, moe_error_bounds_t *out);
 int32_t moe_kstar_separated(const double *V, int32_t kmax, double a, double delta);
 
 /*
+ * Least-squares fit of one layer's expert-operation time on passes with chosen ids
+ * [Lan, §2 "Effective bandwidth", fit (4): t_slot = t_op + c_u U b + c_re (n m - U) b, with
+ * c_re / c_u the re-read cost; App. E "Deduplicating fit", (E.1): t_dedup = t_op + c_g U b +
+ * c_t n].  Host only.
+ *   count          passes (>= 3); n, U [host] int32 [count]: tokens and distinct experts of
+ *                  each pass; t [host] double [count]: its (median) operation time.
+ *   m, b           experts per token, bytes of one expert of the timed layer.
+ *   form           0: per-slot fit (4), coef = {t_op, c_u, c_re};
+ *                  1: deduplicating fit (E.1), coef = {t_op, c_g, c_t}.
+ *   coef           [host] double [3] out.
+ * Returns MOE_ERR_ARG for bad arguments or a design matrix of rank below 3 (e.g. every pass
+ * with the same n and U).
+ */
+moe_status_t moe_fit_op_times(int32_t count, const int32_t *n, const int32_t *U, const double *t, int32_t m,
+                              double b, int32_t form, double *coef);
+
+/*
  * Synchronises stream s, reads the device error word of the workspace [dev] into *code
  * (a moe_status_t value; MOE_OK if nothing was recorded) and clears it.
  */

@@ -60,7 +60,7 @@ EXPORTED = ("moe_abi_version", "moe_status_str", "moe_workspace_bytes", "moe_wor
             "moe_pass_bytes", "moe_bandwidth_report", "moe_expected_union",
             "moe_best_draft_length", "moe_last_device_error", "moe_expert_op_perslot_noalloc",
             "moe_staircase", "moe_speedup", "moe_reuse_threshold", "moe_reuse_threshold_bytes",
-            "moe_error_bounds", "moe_kstar_separated")
+            "moe_error_bounds", "moe_kstar_separated", "moe_fit_op_times")
 
 _lib = None
 
@@ -101,6 +101,7 @@ def lib():
         "moe_reuse_threshold_bytes": ([I32, D, D, D, D], D),
         "moe_error_bounds": ([D, ctypes.POINTER(_ErrorBounds)], I32),
         "moe_kstar_separated": ([P, I32, D, D], I32),
+        "moe_fit_op_times": ([I32, P, P, P, I32, D, I32, P], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -324,3 +325,15 @@ def kstar_separated(V, a: float, delta: float) -> bool:
     if r < 0:
         raise MoeError(1, "moe_kstar_separated")
     return bool(r)
+
+
+def fit_op_times(n, U, t, m: int, b: float, form: str) -> tuple:
+    """Fit (4) (form 'slot': t_op, c_u, c_re) or (E.1) (form 'dedup': t_op, c_g, c_t)."""
+    n = np.ascontiguousarray(np.asarray(n, dtype=np.int32))
+    U = np.ascontiguousarray(np.asarray(U, dtype=np.int32))
+    t = np.ascontiguousarray(np.asarray(t, dtype=np.float64))
+    coef = np.zeros(3, np.float64)
+    _check(lib().moe_fit_op_times(n.size, ctypes.c_void_p(n.ctypes.data), ctypes.c_void_p(U.ctypes.data),
+                                  ctypes.c_void_p(t.ctypes.data), int(m), float(b), 0 if form == "slot" else 1,
+                                  ctypes.c_void_p(coef.ctypes.data)), "moe_fit_op_times")
+    return tuple(float(c) for c in coef)

@@ -397,6 +397,56 @@ int32_t moe_kstar_separated(const double *V, int32_t kmax, double a, double delt
     return 1;
 }
 
+moe_status_t moe_fit_op_times(int32_t count, const int32_t *n, const int32_t *U, const double *t, int32_t m,
+                              double b, int32_t form, double *coef) {
+    if (count < 3 || n == nullptr || U == nullptr || t == nullptr || coef == nullptr || m < 1 || !(b > 0.0) ||
+        (form != 0 && form != 1))
+        return MOE_ERR_ARG;
+    // columns of the design matrix, each scaled to unit norm, then a modified Gram-Schmidt QR
+    const size_t C = static_cast<size_t>(count);
+    std::vector<double> A(3 * C);
+    for (size_t r = 0; r < C; ++r) {
+        if (n[r] < 1 || U[r] < 0 || !std::isfinite(t[r])) return MOE_ERR_ARG;
+        A[r] = 1.0;
+        A[C + r] = static_cast<double>(U[r]) * b;
+        A[2 * C + r] = form == 0 ? (static_cast<double>(n[r]) * m - U[r]) * b : static_cast<double>(n[r]);
+    }
+    double scale[3], R[3][3] = {{0.0}}, qt[3];
+    for (int j = 0; j < 3; ++j) {
+        double nn = 0.0;
+        for (size_t r = 0; r < C; ++r) nn += A[j * C + r] * A[j * C + r];
+        scale[j] = std::sqrt(nn);
+        if (!(scale[j] > 0.0)) return MOE_ERR_ARG;
+        for (size_t r = 0; r < C; ++r) A[j * C + r] /= scale[j];
+    }
+    std::vector<double> y(t, t + C);
+    for (int j = 0; j < 3; ++j) {
+        for (int i = 0; i < j; ++i) {
+            double dot = 0.0;
+            for (size_t r = 0; r < C; ++r) dot += A[i * C + r] * A[j * C + r];
+            R[i][j] = dot;
+            for (size_t r = 0; r < C; ++r) A[j * C + r] -= dot * A[i * C + r];
+        }
+        double nn = 0.0;
+        for (size_t r = 0; r < C; ++r) nn += A[j * C + r] * A[j * C + r];
+        R[j][j] = std::sqrt(nn);
+        if (!(R[j][j] > 1e-10)) return MOE_ERR_ARG;   // rank below 3
+        for (size_t r = 0; r < C; ++r) A[j * C + r] /= R[j][j];
+        double dot = 0.0;
+        for (size_t r = 0; r < C; ++r) dot += A[j * C + r] * y[r];
+        qt[j] = dot;
+        for (size_t r = 0; r < C; ++r) y[r] -= dot * A[j * C + r];
+    }
+    double x[3];
+    for (int j = 2; j >= 0; --j) {
+        double v = qt[j];
+        for (int k = j + 1; k < 3; ++k) v -= R[j][k] * x[k];
+        x[j] = v / R[j][j];
+    }
+    for (int j = 0; j < 3; ++j) coef[j] = x[j] / scale[j];
+    return MOE_OK;
+}
+
 moe_status_t moe_last_device_error(void *ws, moe_stream_t s, int32_t *code) {
     if (ws == nullptr || code == nullptr) return MOE_ERR_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(s);

@@ -12,6 +12,11 @@ Laws (the input recipe):
     previous token's set independently with probability rho and fills the rest with a
     uniform draw without replacement from the experts it did not keep.  rho = 0 is
     independent uniform routing.
+  * chosen ids      a pass of n tokens whose n*m slots name exactly U distinct experts
+    (m <= U <= min(N, n*m)): a uniform U-subset of the experts in random order, token t
+    taking the m consecutive entries starting at position t*m (cyclically), so that every
+    token's m experts are distinct and together they cover all U; then each token's order
+    is shuffled.
   * router logits   z ~ N(0, 1) per token, then every expert outside the token's set is
     shifted down by one common amount per token, so that the set is exactly the top-m
     of the logits with a margin of at least 0.25; the logits of the selected experts
@@ -69,6 +74,19 @@ def routing_traces(L: int, T: int, N: int, m: int, rho: float, seed: int):
     shift = np.where(np.isfinite(shift), shift, 0.0)
     logits = np.where(member, z, z - shift[..., None]).astype(np.float32)
     return sets, logits
+
+
+def chosen_ids(n: int, m: int, N: int, U: int, seed: int) -> np.ndarray:
+    """ids [n, m] int32 of a pass whose slots name exactly U distinct experts."""
+    if not (m <= U <= min(N, n * m)):
+        raise ValueError(f"U={U} outside [m, min(N, n*m)] = [{m}, {min(N, n * m)}]")
+    rng = np.random.default_rng(seed)
+    E = rng.permutation(N)[:U]
+    ids = np.empty((n, m), dtype=np.int32)
+    for t in range(n):
+        ids[t] = E[(t * m + np.arange(m)) % U]
+        rng.shuffle(ids[t])
+    return ids
 
 
 def expert_weights(N: int, f: int, d: int, dtype: torch.dtype, seed: int,

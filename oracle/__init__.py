@@ -332,3 +332,30 @@ def err_speedup_interval(delta):
     hi = np.zeros(1, np.float64)
     _load().oracle_err_speedup_interval(float(delta), _ptr(lo), _ptr(hi))
     return float(lo[0]), float(hi[0])
+
+
+# ---------------------------------------------------------------- operation-time fits
+def fit_slot(n, U, t, m: int, b: float):
+    """Least-squares fit (4) of the per-slot operation time on passes with chosen ids
+    [Lan, §2 "Effective bandwidth"]: t = t_op + c_u U b + c_re (n m - U) b.
+    Returns (t_op, c_u, c_re)."""
+    n, U, t = (np.asarray(v, dtype=np.float64) for v in (n, U, t))
+    A = np.stack([np.ones_like(U), U * b, (n * m - U) * b], axis=1)
+    coef, *_ = np.linalg.lstsq(A, t, rcond=None)
+    return tuple(float(c) for c in coef)
+
+
+def fit_dedup(n, U, t, b: float):
+    """Least-squares fit (E.1) of the deduplicating operation time on passes with chosen ids
+    [Lan, App. E "Deduplicating fit"]: t = t_op + c_g U b + c_t n.  Returns (t_op, c_g, c_t)."""
+    n, U, t = (np.asarray(v, dtype=np.float64) for v in (n, U, t))
+    A = np.stack([np.ones_like(U), U * b, n], axis=1)
+    coef, *_ = np.linalg.lstsq(A, t, rcond=None)
+    return tuple(float(c) for c in coef)
+
+
+def fit_error(predicted, measured) -> float:
+    """A fit's error on windows of recorded routing [Lan, §4: the median relative error of
+    the fit's time on the windows it did not see]."""
+    p, q = np.asarray(predicted, np.float64), np.asarray(measured, np.float64)
+    return float(np.median(np.abs(p - q) / q))

@@ -216,3 +216,19 @@ def test_error_bounds_and_separation_match_oracle(lib, oracle_mod):
         api.staircase([1.0])
     with pytest.raises(api.MoeError):
         api.staircase([1.0, -2.0])
+
+
+def test_fit_op_times_matches_oracle(lib, oracle_mod):
+    rng = np.random.default_rng(63)
+    m, b = 8, 9.437184e6
+    for _ in range(50):
+        n = np.repeat(np.arange(2, 17), 4)
+        U = np.array([int(rng.integers(m, min(128, k * m) + 1)) for k in n])
+        t = 1e-5 + 1.3e-13 * U * b + 0.4e-13 * (n * m - U) * b
+        t = t * (1 + rng.normal(0, 0.03, t.size))
+        for form, fit in (("slot", lambda: oracle_mod.fit_slot(n, U, t, m, b)), ("dedup", lambda: oracle_mod.fit_dedup(n, U, t, b))):
+            got, want = api.fit_op_times(n, U, t, m, b, form), fit()
+            for g_, w_ in zip(got, want):
+                assert g_ == pytest.approx(w_, rel=1e-7, abs=1e-22)
+    with pytest.raises(api.MoeError):
+        api.fit_op_times([2, 2, 2], [8, 8, 8], [1.0, 1.0, 1.0], m, b, "slot")   # rank 1

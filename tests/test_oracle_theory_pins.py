@@ -268,3 +268,44 @@ def test_error_bound_factor_at_ten_percent(oracle_mod):
     assert hi == pytest.approx(1.25, rel=1e-14) and lo == pytest.approx(0.8, rel=1e-14)
     assert oracle_mod.err_decision_agrees(1.0, 0.8, 0.1) is True     # |ln 1.25| > ln(1.1/0.9)
     assert oracle_mod.err_decision_agrees(1.0, 0.85, 0.1) is False
+
+
+# ------------------------------------------------------------------ chosen ids and fits
+
+def test_chosen_ids_name_exactly_U_experts(oracle_mod):
+    from moe_speculative_decoding_gb300 import synth
+    rng = np.random.default_rng(110)
+    for _ in range(300):
+        N, m = int(rng.integers(2, 130)), 0
+        m = int(rng.integers(1, min(N, 9) + 1))
+        n = int(rng.integers(1, 17))
+        U = int(rng.integers(m, min(N, n * m) + 1))
+        ids = synth.chosen_ids(n, m, N, U, seed=int(rng.integers(1 << 30)))
+        assert ids.shape == (n, m) and ids.min() >= 0 and ids.max() < N
+        assert all(len(set(row)) == m for row in ids.tolist())
+        assert len(set(ids.ravel().tolist())) == U
+        assert oracle_mod.pass_bytes(64, 64, N, ids)["U"] == U
+    with pytest.raises(ValueError):
+        synth.chosen_ids(2, 4, 128, 3, 0)
+
+
+def test_fits_recover_known_coefficients(oracle_mod):
+    """(4) and (E.1) on noise-free times built from known constants return them; on noisy
+    times the residual is orthogonal to every regressor (least squares)."""
+    rng = np.random.default_rng(111)
+    m, b = 8, 9.437184e6
+    n = np.repeat(np.arange(2, 10), 5)
+    U = np.array([int(rng.integers(m, n_ * m + 1)) for n_ in n])
+    t_op, cu, cre = 12e-6, 1.4e-13, 0.3e-13
+    t = t_op + cu * U * b + cre * (n * m - U) * b
+    got = oracle_mod.fit_slot(n, U, t, m, b)
+    assert got == pytest.approx((t_op, cu, cre), rel=1e-9)
+    tg, cg, ct = 9e-6, 1.6e-13, 2e-7
+    got = oracle_mod.fit_dedup(n, U, tg + cg * U * b + ct * n, b)
+    assert got == pytest.approx((tg, cg, ct), rel=1e-9)
+    noisy = t * (1 + rng.normal(0, 0.02, t.size))
+    c = oracle_mod.fit_slot(n, U, noisy, m, b)
+    res = noisy - (c[0] + c[1] * U * b + c[2] * (n * m - U) * b)
+    for col in (np.ones_like(U), U * b, (n * m - U) * b):
+        assert abs(np.dot(res, col)) <= 1e-9 * np.linalg.norm(col) * np.linalg.norm(noisy)
+    assert oracle_mod.fit_error([1.1, 0.9, 1.0], [1.0, 1.0, 1.0]) == pytest.approx(0.1)
