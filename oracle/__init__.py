@@ -74,6 +74,12 @@ def _load():
             fn.argtypes = args
             fn.restype = D
         lib.oracle_step_points.argtypes = [P, I, P]
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = D
+        lib.oracle_e4m3_encode.argtypes = [D]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_quantize_rows_e4m3.argtypes = [P, I, I, I, P, P]
+        lib.oracle_expert_op_token_fp8.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P, P, P, I, P]
         lib.oracle_convex_nondecreasing.argtypes = [P, I]
         lib.oracle_err_decision_agrees.argtypes = [D, D, D]
         lib.oracle_err_kstar_separated.argtypes = [P, I, D, D]
@@ -359,3 +365,41 @@ def fit_error(predicted, measured) -> float:
     the fit's time on the windows it did not see]."""
     p, q = np.asarray(predicted, np.float64), np.asarray(measured, np.float64)
     return float(np.median(np.abs(p - q) / q))
+
+
+# ---------------------------------------------------------------- FP8 (e4m3) experts
+def e4m3_decode(c: int) -> float:
+    return float(_load().oracle_e4m3_decode(int(c)))
+
+
+def e4m3_encode(v: float) -> int:
+    return int(_load().oracle_e4m3_encode(float(v)))
+
+
+def quantize_rows_e4m3(src: np.ndarray):
+    """src [rows, cols] float32 or bf16-as-uint16 -> (codes uint8 [rows, cols], scale float32 [rows])."""
+    src = np.ascontiguousarray(src)
+    rows, cols = src.shape
+    q = np.zeros((rows, cols), np.uint8)
+    sc = np.zeros(rows, np.float32)
+    _load().oracle_quantize_rows_e4m3(_ptr(src), _wcode(src), rows, cols, _ptr(q), _ptr(sc))
+    return q, sc
+
+
+def expert_op_token_fp8(wg, wu, wd, sg, su, sd, x, sx, ids, gates, t):
+    """y_t [d] of the e4m3 expert operation; weights [E, f, d] / [E, d, f] uint8 codes with
+    row scales [E, f] / [E, d]; x [n, d] codes with row scales sx [n]; ids index the E experts."""
+    E, f, d = wg.shape
+    arrs = [np.ascontiguousarray(a) for a in (wg, wu, wd)]
+    scs = [np.ascontiguousarray(a, dtype=np.float32) for a in (sg, su, sd)]
+    x = np.ascontiguousarray(x, dtype=np.uint8)
+    sx = np.ascontiguousarray(sx, dtype=np.float32)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    gates = np.ascontiguousarray(gates, dtype=np.float64)
+    y = np.zeros(d, np.float64)
+    rc = _load().oracle_expert_op_token_fp8(d, f, E, ids.shape[1], *[_ptr(a) for a in arrs],
+                                            *[_ptr(a) for a in scs], _ptr(x), _ptr(sx), _ptr(ids),
+                                            _ptr(gates), int(t), _ptr(y))
+    if rc != 0:
+        raise ValueError("oracle_expert_op_token_fp8: bad arguments")
+    return y

@@ -31,6 +31,10 @@
  *   oracle_reuse_threshold*  the pages' counterexample (rho*_1 = 7/20, rho*_2 = 371/800 and
  *                            its three patterns); identity (B.13); brute-force speedups
  *   oracle_err_*             random perturbations of every bandwidth within the bound
+ *   oracle_e4m3_*            every code against torch.float8_e4m3fn; nearest-value search
+ *   oracle_quantize_rows_e4m3 the definition: scale = amax/448, codes round to nearest
+ *   oracle_expert_op_token_fp8 the fp64 SwiGLU of the dequantized weights within the
+ *                            rounding bound of the quantized h (2^-4 relative)
  */
 #include <math.h>
 #include <stdint.h>
@@ -630,4 +634,118 @@ void oracle_err_speedup_interval(double delta, double *lo, double *hi)
 {
     *lo = (1.0 - delta) / (1.0 + delta);
     *hi = (1.0 + delta) / (1.0 - delta);
+}
+
+/* ------------------------------------------------------------------ FP8 (e4m3) experts */
+
+/*
+ * OCP FP8 E4M3 ("FN": no infinities): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+ * bits.  Exponent 0: subnormal, m * 2^-9.  Exponent 1..15: 2^(e-7) (1 + m/8), except
+ * exponent 15 with mantissa 7, which is NaN.  Largest finite value 448.
+ */
+double oracle_e4m3_decode(uint8_t c)
+{
+    int sgn = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = (double)m * ldexp(1.0, -9);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sgn ? -v : v;
+}
+
+/*
+ * The e4m3 code nearest to v: a search over every finite code, ties to the even mantissa
+ * (the code with the lower mantissa bit clear); |v| above 448 saturates to +-448 (the
+ * saturating conversion).  v must not be NaN.
+ */
+uint8_t oracle_e4m3_encode(double v)
+{
+    int sgn = v < 0.0 || (v == 0.0 && signbit(v));
+    double a = fabs(v);
+    int best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c < 127; ++c) {   /* codes 0..126: +0 .. 448, 127 is NaN */
+        double d = fabs(oracle_e4m3_decode((uint8_t)c) - a);
+        if (d < bd || (d == bd && (c & 1) == 0)) { bd = d; best = c; }
+    }
+    return (uint8_t)(best | (sgn << 7));
+}
+
+/*
+ * Per-row quantization to e4m3 (the format the tensor-core FP8 path reads): for each row,
+ * amax = max |v|, scale = amax / 448 in fp32 (1 when amax = 0), codes = e4m3(v / scale)
+ * with the division in fp32.  The division and the scale are taken in the kernel's
+ * precision, fp32, because they decide integer codes.
+ *   src [rows, cols] fp32 (dtype 0) or bf16 bits (dtype 1); q [rows, cols]; scale [rows].
+ */
+int oracle_quantize_rows_e4m3(const void *src, int dtype, int rows, int cols, uint8_t *q, float *scale)
+{
+    for (int r = 0; r < rows; ++r) {
+        float amax = 0.0f;
+        for (int c = 0; c < cols; ++c) {
+            float v = (float)widen(src, dtype, (size_t)r * cols + c);
+            if (fabsf(v) > amax) amax = fabsf(v);
+        }
+        float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scale[r] = sc;
+        for (int c = 0; c < cols; ++c) {
+            float v = (float)widen(src, dtype, (size_t)r * cols + c);
+            q[(size_t)r * cols + c] = oracle_e4m3_encode((double)(v / sc));
+        }
+    }
+    return 0;
+}
+
+/*
+ * The expert operation of one token with e4m3 weights and activations (the quantized
+ * experts of [Lan], App. E Table 6, on GB300's FP8 format).  For each of token t's m
+ * experts e:
+ *   g_i = sg[e][i] sx[t] sum_k W_g[e][i][k] x[t][k],  u_i the same with W_u, sigma = silu;
+ *   h_i = silu(g_i) u_i, quantized per block of 128 consecutive i: s_b = amax_b / 448 in
+ *   fp32, h~_i = e4m3(h_i / s_b) s_b (the down projection's operand);
+ *   y_t[o] += gates[t][j] sd[e][o] sum_i W_d[e][o][i] h~_i.
+ * W_g, W_u [N][f][d], W_d [N][d][f] e4m3 codes; sg, su [N][f], sd [N][d] fp32; x [n][d]
+ * codes, sx [n].  f must be a multiple of 128.  Returns 0, or -1 for bad arguments.
+ */
+int oracle_expert_op_token_fp8(int d, int f, int N, int m, const uint8_t *wg, const uint8_t *wu,
+                               const uint8_t *wd, const float *sg, const float *su, const float *sd,
+                               const uint8_t *x, const float *sx, const int32_t *ids, const double *gates,
+                               int t, double *y_t)
+{
+    if (f % 128 != 0) return -1;
+    double *h = (double *)malloc(sizeof(double) * (size_t)f);
+    double *hq = (double *)malloc(sizeof(double) * (size_t)f);
+    if (!h || !hq) { free(h); free(hq); return -1; }
+    for (int o = 0; o < d; ++o) y_t[o] = 0.0;
+    for (int j = 0; j < m; ++j) {
+        int e = ids[(size_t)t * m + j];
+        if (e < 0 || e >= N) { free(h); free(hq); return -1; }
+        for (int i = 0; i < f; ++i) {
+            double g = 0.0, u = 0.0;
+            for (int k = 0; k < d; ++k) {
+                double xv = oracle_e4m3_decode(x[(size_t)t * d + k]);
+                g += oracle_e4m3_decode(wg[((size_t)e * f + i) * d + k]) * xv;
+                u += oracle_e4m3_decode(wu[((size_t)e * f + i) * d + k]) * xv;
+            }
+            g *= (double)sg[(size_t)e * f + i] * (double)sx[t];
+            u *= (double)su[(size_t)e * f + i] * (double)sx[t];
+            h[i] = g / (1.0 + exp(-g)) * u;
+        }
+        for (int b0 = 0; b0 < f; b0 += 128) {
+            float amax = 0.0f;
+            for (int i = b0; i < b0 + 128; ++i)
+                if (fabsf((float)h[i]) > amax) amax = fabsf((float)h[i]);
+            float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+            for (int i = b0; i < b0 + 128; ++i)
+                hq[i] = oracle_e4m3_decode(oracle_e4m3_encode((double)((float)h[i] / sc))) * (double)sc;
+        }
+        for (int o = 0; o < d; ++o) {
+            double acc = 0.0;
+            for (int i = 0; i < f; ++i) acc += oracle_e4m3_decode(wd[((size_t)e * d + o) * f + i]) * hq[i];
+            y_t[o] += gates[(size_t)t * m + j] * (double)sd[(size_t)e * d + o] * acc;
+        }
+    }
+    free(h);
+    free(hq);
+    return 0;
 }
