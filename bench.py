@@ -27,6 +27,7 @@ roofline = the expert kernel: requested bytes per launch / its mean launch time,
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
@@ -63,6 +64,7 @@ def parse():
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-fit", action="store_true", help="skip the chosen-id fits (4) and (E.1)")
+    p.add_argument("--no-fp8", action="store_true", help="skip the e4m3 (FP8) expert step")
     p.add_argument("--fit-only", action="store_true",
                    help="only the chosen-id fits, on one freshly generated layer (prints their JSON)")
     p.add_argument("--fit-reps", type=int, default=7)
@@ -187,6 +189,131 @@ def step_time_theory(n_values, Vs, Vd, Vw, bytes_slot, bytes_dedup, K):
     eb = api.error_bounds(0.10)
     out["error_bounds_eps_0.10"] = {k: round(v, 6) for k, v in eb.items()}
     return out
+
+
+def fp8_leg(b: "StackBench", args, device, per_n_bf16):
+    """The same step with e4m3 experts (GB300's FP8 in place of the pages' quantized
+    experts): the stack quantized once, then per n and layer one activation quantization and
+    the FP8 expert operation, per-slot and dedup (the dedup grouping is the bf16 step's, the
+    same kernel on the same ids; its time is added from that run).  Timed over the same
+    windows after the bf16 measurement; value = FP8 expert bytes requested / time."""
+    wl, L = b.wl, b.L
+    layer8 = api.make_layer(wl.d, wl.f, wl.N, wl.m, "e4m3")
+    ws8 = api.workspace(layer8, 16, device)
+    t0 = time.time()
+    w8 = [api.quantize_experts(w) for w in b.weights]
+    torch.cuda.synchronize(device)
+    t_quant = time.time() - t0
+    bufs = {}
+    for n in b.n_values:
+        bufs[n] = dict(xq=torch.empty((L, n, wl.d), dtype=torch.uint8, device=device),
+                       sx=torch.empty((L, 16), dtype=torch.float32, device=device),
+                       ys=torch.zeros((L, n, wl.d), dtype=torch.float32, device=device),
+                       yd=torch.zeros((L, n, wl.d), dtype=torch.float32, device=device))
+
+    def slot8(n):
+        st, bf = b.per_n[n], bufs[n]
+        for l in range(L):
+            xq, sx = bf["xq"][l], bf["sx"][l, :n]
+            api._check(api.lib().moe_quantize_rows_e4m3(ctypes.c_void_p(st["x"].data_ptr()), api.MOE_BF16, n, wl.d,
+                                                        ctypes.c_void_p(xq.data_ptr()), ctypes.c_void_p(sx.data_ptr()),
+                                                        api._stream(device)), "moe_quantize_rows_e4m3")
+            api.expert_op_perslot_fp8(layer8, w8[l][0], w8[l][1], xq, sx, st["ids"][l * n:(l + 1) * n],
+                                      st["gates"][l * n:(l + 1) * n], y=bf["ys"][l], accumulate=True, ws=ws8)
+
+    def dedup8(n):
+        st, bf = b.per_n[n], bufs[n]
+        for l in range(L):
+            xq, sx = bf["xq"][l], bf["sx"][l, :n]
+            api._check(api.lib().moe_quantize_rows_e4m3(ctypes.c_void_p(st["x"].data_ptr()), api.MOE_BF16, n, wl.d,
+                                                        ctypes.c_void_p(xq.data_ptr()), ctypes.c_void_p(sx.data_ptr()),
+                                                        api._stream(device)), "moe_quantize_rows_e4m3")
+            api.expert_op_dedup_fp8(layer8, w8[l][0], w8[l][1], xq, sx, st["gates"][l * n:(l + 1) * n],
+                                    st["groups"][l], y=bf["yd"][l], accumulate=True, ws=ws8)
+
+    graphs = {}
+    for n in b.n_values:
+        slot8(n), dedup8(n)
+        torch.cuda.synchronize(device)
+        for ph, fn in (("slot8", slot8), ("dedup8", dedup8)):
+            if b.use_graph:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    fn(n)
+                graphs[(n, ph)] = g
+            else:
+                graphs[(n, ph)] = (lambda fn=fn, n=n: fn(n))
+
+    def run(n, ph):
+        g = graphs[(n, ph)]
+        g.replay() if b.use_graph else g()
+
+    def step(w, ev=None):
+        for n in b.n_values:
+            b.stage(n, w)
+            b._run(n, "route")
+            b._run(n, "group")
+            bufs[n]["ys"].zero_()
+            bufs[n]["yd"].zero_()
+            if ev is not None:
+                ev[(n, "start")].record()
+            for ph in ("slot8", "dedup8"):
+                run(n, ph)
+                if ev is not None:
+                    ev[(n, ph)].record()
+
+    for w in range(args.warmup):
+        step(w)
+    torch.cuda.synchronize(device)
+    K = args.steps
+    evs = [{(n, k): torch.cuda.Event(enable_timing=True) for n in b.n_values for k in ("start", "slot8", "dedup8")}
+           for _ in range(K)]
+    for k in range(K):
+        step(args.warmup + k, evs[k])
+    torch.cuda.synchronize(device)
+    assert api.last_device_error(ws8) == 0
+    tot_b, tot_t, rows = 0.0, 0.0, []
+    bf16 = {r["n"]: r for r in per_n_bf16}
+    for n in b.n_values:
+        ts = sum(evs[k][(n, "start")].elapsed_time(evs[k][(n, "slot8")]) * 1e-3 for k in range(K))
+        td = sum(evs[k][(n, "slot8")].elapsed_time(evs[k][(n, "dedup8")]) * 1e-3 for k in range(K))
+        bs = bd = 0
+        for k in range(K):
+            w = args.warmup + k
+            for l in range(L):
+                pb = api.pass_bytes(layer8, b.sets[l, w * n:(w + 1) * n])
+                bs += pb["slot_bytes"]
+                bd += pb["dedup_bytes"]
+        tg = bf16[n]["us_dedup_group"] * 1e-6 * K
+        tot_b += bs + bd
+        tot_t += ts + td + tg
+        rows.append(dict(n=n, us_slot=round(ts / K * 1e6, 2), us_dedup=round((td + tg) / K * 1e6, 2),
+                         tbps_slot=round(bs / ts / 1e12, 3), tbps_dedup_kernel=round(bd / td / 1e12, 3),
+                         speedup_slot=round(bf16[n]["us_slot"] / (ts / K * 1e6), 3),
+                         speedup_dedup=round(bf16[n]["us_dedup"] / ((td + tg) / K * 1e6), 3)))
+    # outputs against the bf16 per-slot pass of the same (last) window: quantization error only;
+    # the FP8 forms against each other: accumulation order only
+    worst, worst_forms = 0.0, 0.0
+    for n in b.n_values:
+        b.stage(n, args.warmup + K - 1)
+        b._run(n, "route")
+        b._run(n, "slot")
+        bufs[n]["ys"].zero_()
+        bufs[n]["yd"].zero_()
+        b._run(n, "group")
+        run(n, "slot8")
+        run(n, "dedup8")
+        torch.cuda.synchronize(device)
+        yb = b.per_n[n]["y_slot"].double()
+        y8, y8d = bufs[n]["ys"].double(), bufs[n]["yd"].double()
+        rms8 = y8.pow(2).mean().sqrt().clamp_min(1e-30)
+        worst = max(worst, float((y8 - yb).pow(2).mean().sqrt() / yb.pow(2).mean().sqrt().clamp_min(1e-30)))
+        worst_forms = max(worst_forms, float((y8 - y8d).abs().max() / rms8))
+    return dict(value=round(tot_b / tot_t / 1e12, 4), unit="TB/s", dtype="e4m3 weights and activations, fp32 accumulate",
+                expert_bytes=int(api.pass_bytes(layer8, b.sets[0, :1])["expert_bytes"]),
+                quantize_s=round(t_quant, 2), per_n=rows, rel_rms_vs_bf16=round(worst, 5),
+                max_dev_dedup_vs_slot=round(worst_forms, 6),
+                launches_per_layer_form=3)
 
 
 def fit_leg(wl, weights, device, reps: int = 7, windows: int = 8, n_max: int = 16):
@@ -506,6 +633,8 @@ def run_ours(args, world, rank, local):
 
     if not args.no_e2e:
         line["e2e"] = e2e_run(b, args, world, device, total_bytes_per_step=total_bytes / K)
+    if not args.no_fp8:
+        line["fp8"] = fp8_leg(b, args, device, per_n)
     if rank == 0 and not args.no_fit:
         line["fits"] = fit_leg(wl, b.weights[0], device, reps=args.fit_reps)
     if rank == 0 and not args.no_cpu_baseline and world == 1:

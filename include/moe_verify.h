@@ -52,7 +52,7 @@ typedef enum {
     MOE_ERR_DEVICE_TIMEOUT = 6  /* (device) a pipeline wait gave up after its time limit */
 } moe_status_t;
 
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2 } moe_dtype_t;
 
 /*
  * One MoE layer [Lan, §1: N experts, each token routed to m of them].
@@ -61,9 +61,11 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
  * Weight layouts (row-major, one contiguous block per expert, nn.Linear convention):
  *   w_gate, w_up  [N, f, d];   w_down  [N, d, f].
  * Supported: 1 <= m <= N <= 1024, d and f multiples of 64, d <= 8192, f <= 65536;
- * (w_dtype, x_dtype) = (MOE_BF16, MOE_BF16) or (MOE_F32, MOE_F32).  The tensor-core
- * kernel takes bf16 layers with d a multiple of 128 and d <= 4096; other bf16 shapes
- * run on the CUDA-core kernel.
+ * (w_dtype, x_dtype) = (MOE_BF16, MOE_BF16), (MOE_F32, MOE_F32) or (MOE_E4M3, MOE_E4M3).
+ * The tensor-core kernels take bf16 layers with d a multiple of 128; other bf16 shapes run
+ * on the CUDA-core kernel.  e4m3 layers (OCP FP8 E4M3 codes, one fp32 scale per weight row
+ * and per token, see moe_quantize_rows_e4m3) run only through the _fp8 calls, on the
+ * tensor cores, with d and f multiples of 128.
  */
 typedef struct {
     int32_t d, f, N, m;
@@ -199,10 +201,53 @@ moe_status_t moe_expert_op_perslot_noalloc(const moe_layer_t *layer, const void 
                                            int32_t *status_out, moe_stream_t s);
 
 /*
+ * FP8 expert weights: the fp32 scale of every weight row [dev]: gate [N, f], up [N, f],
+ * down [N, d] (value = code * scale; see moe_quantize_rows_e4m3).
+ */
+typedef struct {
+    const float *gate, *up, *down;
+} moe_weight_scales_t;
+
+/*
+ * The per-slot and the deduplicating expert operation of an e4m3 layer (the quantized
+ * experts of [Lan, App. E Table 6], in GB300's FP8 tensor-core format): as
+ * moe_expert_op_perslot / moe_expert_op_dedup, with
+ *   w_gate, w_up, w_down [dev] e4m3 codes in the layouts of moe_layer_t, scales their row scales;
+ *   x [dev] uint8 [n, d] e4m3 codes, x_scale [dev] fp32 [n] the token scales (scale arrays
+ *   need only 4-byte alignment; every other pointer 16 bytes, as elsewhere).
+ * h is rounded to e4m3 as the down projection's operand, with one scale per token and
+ * 128-wide block of f (amax / 448).  layer->w_dtype = layer->x_dtype = MOE_E4M3, d and f
+ * multiples of 128; requested bytes per expert w = 3 d f + 4 (2 f + d) (moe_pass_bytes).
+ * Returns MOE_ERR_UNSUPPORTED for a layer that is not e4m3.
+ */
+moe_status_t moe_expert_op_perslot_fp8(const moe_layer_t *layer, const void *w_gate, const void *w_up,
+                                       const void *w_down, const moe_weight_scales_t *scales, const void *x,
+                                       const float *x_scale, const int32_t *ids, const float *gates, int32_t n,
+                                       int32_t accumulate, float *y, void *ws, size_t ws_bytes, moe_stream_t s);
+
+moe_status_t moe_expert_op_dedup_fp8(const moe_layer_t *layer, const void *w_gate, const void *w_up,
+                                     const void *w_down, const moe_weight_scales_t *scales, const void *x,
+                                     const float *x_scale, const float *gates, int32_t n, const int32_t *num_distinct,
+                                     const int32_t *expert_list, const int32_t *expert_offsets,
+                                     const int32_t *slot_order, int32_t accumulate, float *y, void *ws,
+                                     size_t ws_bytes, moe_stream_t s);
+
+/*
+ * Per-row quantization to e4m3 on the device (the operand format of the _fp8 calls): for each
+ * row r of src [rows, cols] (fp32 or bf16 by src_dtype), scale[r] = amax_r / 448 in fp32 (1 if
+ * the row is all zero) and q[r][c] = e4m3(src[r][c] / scale[r]), the division in IEEE fp32,
+ * rounded to nearest with ties to even and saturated at +-448.
+ *   src [dev], q [dev] uint8 [rows, cols], scale [dev] fp32 [rows].  rows == 0 enqueues nothing.
+ */
+moe_status_t moe_quantize_rows_e4m3(const void *src, int32_t src_dtype, int32_t rows, int32_t cols, uint8_t *q,
+                                    float *scale, moe_stream_t s);
+
+/*
  * Requested bytes of one pass [Lan, §1 "Bytes": E_slot = m*n*w, E_dedup = w * X(n);
  * §2 "Effective bandwidth": u_bar(n) = E_dedup / E_slot].  Host only.
  *   ids_host [host] int32 [n*m].
- *   out: expert_bytes w = 3*d*f*sizeof(weight); slot_bytes = n*m*w; dedup_bytes = U*w;
+ *   out: expert_bytes w = 3*d*f*sizeof(weight) (+ 4*(2f + d) row-scale bytes for e4m3);
+ *        slot_bytes = n*m*w; dedup_bytes = U*w;
  *        act_bytes = n*d*sizeof(x) + n*d*4 (activations read, output written; reported
  *        apart and never part of E_slot, E_dedup or u_bar); U; ubar = U / (n*m).
  * Returns MOE_ERR_BAD_ID if an id is outside [0, N).

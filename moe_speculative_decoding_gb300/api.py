@@ -16,7 +16,7 @@ import torch
 
 from . import build as _build
 
-MOE_F32, MOE_BF16 = 0, 1
+MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
 MOE_FLAG_SIMT = 1
 MAX_PASS_TOKENS = 16
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
@@ -36,6 +36,8 @@ class Layer(ctypes.Structure):
 
     @property
     def torch_dtype(self):
+        if self.w_dtype == MOE_E4M3:
+            return torch.uint8   # e4m3 codes
         return torch.bfloat16 if self.w_dtype == MOE_BF16 else torch.float32
 
 
@@ -44,6 +46,10 @@ class _PassBytes(ctypes.Structure):
                 ("dedup_bytes", ctypes.c_uint64), ("act_bytes", ctypes.c_uint64),
                 ("n", ctypes.c_int32), ("m", ctypes.c_int32), ("U", ctypes.c_int32),
                 ("reserved", ctypes.c_int32), ("ubar", ctypes.c_double)]
+
+
+class WeightScales(ctypes.Structure):
+    _fields_ = [("gate", ctypes.c_void_p), ("up", ctypes.c_void_p), ("down", ctypes.c_void_p)]
 
 
 class ThresholdIn(ctypes.Structure):
@@ -60,7 +66,8 @@ EXPORTED = ("moe_abi_version", "moe_status_str", "moe_workspace_bytes", "moe_wor
             "moe_pass_bytes", "moe_bandwidth_report", "moe_expected_union",
             "moe_best_draft_length", "moe_last_device_error", "moe_expert_op_perslot_noalloc",
             "moe_staircase", "moe_speedup", "moe_reuse_threshold", "moe_reuse_threshold_bytes",
-            "moe_error_bounds", "moe_kstar_separated", "moe_fit_op_times")
+            "moe_error_bounds", "moe_kstar_separated", "moe_fit_op_times", "moe_expert_op_perslot_fp8",
+            "moe_expert_op_dedup_fp8", "moe_quantize_rows_e4m3")
 
 _lib = None
 
@@ -102,6 +109,11 @@ def lib():
         "moe_error_bounds": ([D, ctypes.POINTER(_ErrorBounds)], I32),
         "moe_kstar_separated": ([P, I32, D, D], I32),
         "moe_fit_op_times": ([I32, P, P, P, I32, D, I32, P], I32),
+        "moe_expert_op_perslot_fp8": ([LP, P, P, P, ctypes.POINTER(WeightScales), P, P, P, P, I32, I32, P, P, SZ, P],
+                                      I32),
+        "moe_expert_op_dedup_fp8": ([LP, P, P, P, ctypes.POINTER(WeightScales), P, P, P, I32, P, P, P, P, I32, P,
+                                     P, SZ, P], I32),
+        "moe_quantize_rows_e4m3": ([P, I32, I32, I32, P, P, P], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -135,7 +147,7 @@ def _dev(t: torch.Tensor, name: str, dtype=None, shape=None):
 # ---------------------------------------------------------------- layer + workspace
 
 def make_layer(d: int, f: int, N: int, m: int, dtype: str = "bf16", simt: bool = False) -> Layer:
-    code = MOE_BF16 if dtype == "bf16" else MOE_F32
+    code = {"bf16": MOE_BF16, "f32": MOE_F32, "e4m3": MOE_E4M3}[dtype]
     return Layer(d, f, N, m, code, code, MOE_FLAG_SIMT if simt else 0)
 
 
@@ -337,3 +349,68 @@ def fit_op_times(n, U, t, m: int, b: float, form: str) -> tuple:
                                   ctypes.c_void_p(t.ctypes.data), int(m), float(b), 0 if form == "slot" else 1,
                                   ctypes.c_void_p(coef.ctypes.data)), "moe_fit_op_times")
     return tuple(float(c) for c in coef)
+
+
+# ---------------------------------------------------------------- FP8 (e4m3) experts
+def quantize_rows_e4m3(src: torch.Tensor):
+    """Row-wise e4m3 codes (uint8, same shape) and fp32 row scales of a 2-D or 3-D fp32/bf16
+    CUDA tensor (rows = all leading dimensions)."""
+    if src.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("quantize_rows_e4m3 takes fp32 or bf16")
+    cols = src.shape[-1]
+    rows = src.numel() // cols
+    q = torch.empty(src.shape, dtype=torch.uint8, device=src.device)
+    scale = torch.empty(src.shape[:-1], dtype=torch.float32, device=src.device)
+    _check(lib().moe_quantize_rows_e4m3(_dev(src, "src"), MOE_F32 if src.dtype == torch.float32 else MOE_BF16,
+                                        rows, cols, ctypes.c_void_p(q.data_ptr()),
+                                        ctypes.c_void_p(scale.data_ptr()), _stream(src.device)),
+           "moe_quantize_rows_e4m3")
+    return q, scale
+
+
+def quantize_experts(weights):
+    """(w_gate, w_up, w_down) bf16/fp32 -> (codes, row scales) for an e4m3 layer."""
+    qs = [quantize_rows_e4m3(w) for w in weights]
+    return tuple(q for q, _ in qs), tuple(s for _, s in qs)
+
+
+def _scales(layer: Layer, scales) -> WeightScales:
+    sg, su, sd = scales
+    return WeightScales(_dev(sg, "s_gate", torch.float32, (layer.N, layer.f)),
+                        _dev(su, "s_up", torch.float32, (layer.N, layer.f)),
+                        _dev(sd, "s_down", torch.float32, (layer.N, layer.d)))
+
+
+def expert_op_perslot_fp8(layer: Layer, weights, scales, xq: torch.Tensor, x_scale: torch.Tensor, ids: torch.Tensor,
+                          gates: torch.Tensor, y=None, accumulate: bool = False, ws=None):
+    n = xq.shape[0]
+    ws = ws if ws is not None else workspace(layer, n, xq.device)
+    y, yp = _y(layer, xq, y)
+    sc = _scales(layer, scales)
+    _check(lib().moe_expert_op_perslot_fp8(ctypes.byref(layer), *_weights(layer, weights), ctypes.byref(sc),
+                                           _dev(xq, "x", torch.uint8, (n, layer.d)),
+                                           _dev(x_scale, "x_scale", torch.float32, (n,)),
+                                           _dev(ids, "ids", torch.int32, (n, layer.m)),
+                                           _dev(gates, "gates", torch.float32, (n, layer.m)), n,
+                                           int(bool(accumulate)), yp, ctypes.c_void_p(ws.data_ptr()),
+                                           ws.numel(), _stream(xq.device)), "moe_expert_op_perslot_fp8")
+    return y
+
+
+def expert_op_dedup_fp8(layer: Layer, weights, scales, xq: torch.Tensor, x_scale: torch.Tensor, gates: torch.Tensor,
+                        grouping: Grouping, y=None, accumulate: bool = False, ws=None):
+    n = xq.shape[0]
+    ws = ws if ws is not None else workspace(layer, n, xq.device)
+    y, yp = _y(layer, xq, y)
+    sc = _scales(layer, scales)
+    _check(lib().moe_expert_op_dedup_fp8(ctypes.byref(layer), *_weights(layer, weights), ctypes.byref(sc),
+                                         _dev(xq, "x", torch.uint8, (n, layer.d)),
+                                         _dev(x_scale, "x_scale", torch.float32, (n,)),
+                                         _dev(gates, "gates", torch.float32, (n, layer.m)), n,
+                                         _dev(grouping.num_distinct, "num_distinct"),
+                                         _dev(grouping.expert_list, "expert_list"),
+                                         _dev(grouping.offsets, "offsets"),
+                                         _dev(grouping.slot_order, "slot_order"),
+                                         int(bool(accumulate)), yp, ctypes.c_void_p(ws.data_ptr()),
+                                         ws.numel(), _stream(xq.device)), "moe_expert_op_dedup_fp8")
+    return y

@@ -18,6 +18,8 @@ cudaError_t launch_route_topm(const float *logits, int n, int N, int m, int reno
                               cudaStream_t s, bool pdl);
 cudaError_t launch_group_slots(const int32_t *ids, int S, int N, int32_t *num_distinct, int32_t *expert_list,
                                int32_t *offsets, int32_t *order, int32_t *err, cudaStream_t s, bool pdl);
+cudaError_t launch_quantize_rows(const void *src, int dtype, int rows, int cols, uint8_t *q, float *scale,
+                                 cudaStream_t s, bool pdl);
 }  // namespace moe
 
 using namespace moe;
@@ -30,8 +32,12 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// the bf16 tensor-core path runs this layer (else the SIMT kernel)
+bool is_fp8(const moe_layer_t *L) { return L->w_dtype == MOE_E4M3 && L->x_dtype == MOE_E4M3; }
+
+// the tensor-core path runs this layer (else the SIMT kernel): bf16 layers it supports, and
+// every e4m3 layer (which has no other path)
 bool uses_tc(const moe_layer_t *L) {
+    if (is_fp8(L)) return true;
     return L->w_dtype == MOE_BF16 && L->x_dtype == MOE_BF16 && !(L->flags & MOE_FLAG_SIMT) &&
            expert_tc_supports(L->d, L->f);
 }
@@ -43,7 +49,8 @@ moe_status_t check_layer(const moe_layer_t *L) {
     if (L->d % 64 != 0 || L->f % 64 != 0 || L->d > 8192 || L->f > 65536) return MOE_ERR_UNSUPPORTED;
     const bool bf = L->w_dtype == MOE_BF16 && L->x_dtype == MOE_BF16;
     const bool fp = L->w_dtype == MOE_F32 && L->x_dtype == MOE_F32;
-    if (!bf && !fp) return MOE_ERR_UNSUPPORTED;
+    if (!bf && !fp && !is_fp8(L)) return MOE_ERR_UNSUPPORTED;
+    if (is_fp8(L) && (L->d % 128 != 0 || L->f % 128 != 0 || (L->flags & MOE_FLAG_SIMT))) return MOE_ERR_UNSUPPORTED;
     if ((L->flags & ~MOE_FLAG_SIMT) != 0) return MOE_ERR_ARG;
     return MOE_OK;
 }
@@ -168,6 +175,7 @@ moe_status_t moe_expert_op_perslot(const moe_layer_t *layer, const void *w_gate,
                                    moe_stream_t s) {
     moe_status_t st = check_expert_common(layer, w_gate, w_up, w_down, x, gates, n, y, ws, ws_bytes);
     if (st != MOE_OK) return st;
+    if (is_fp8(layer)) return MOE_ERR_UNSUPPORTED;   // e4m3 needs its scales: the _fp8 call
     if (ids == nullptr || !aligned16(ids)) return MOE_ERR_ARG;
     ExpertArgs a = make_args(layer, w_gate, w_up, w_down, x, gates, n, y, ws, kModePerSlot);
     a.ids = ids;
@@ -181,6 +189,7 @@ moe_status_t moe_expert_op_dedup(const moe_layer_t *layer, const void *w_gate, c
                                  float *y, void *ws, size_t ws_bytes, moe_stream_t s) {
     moe_status_t st = check_expert_common(layer, w_gate, w_up, w_down, x, gates, n, y, ws, ws_bytes);
     if (st != MOE_OK) return st;
+    if (is_fp8(layer)) return MOE_ERR_UNSUPPORTED;   // e4m3 needs its scales: the _fp8 call
     const void *ptrs[] = {num_distinct, expert_list, expert_offsets, slot_order};
     for (const void *p : ptrs)
         if (p == nullptr || !aligned16(p)) return MOE_ERR_ARG;
@@ -191,6 +200,71 @@ moe_status_t moe_expert_op_dedup(const moe_layer_t *layer, const void *w_gate, c
     a.slot_order = slot_order;
     const int cap = n * layer->m < layer->N ? n * layer->m : layer->N;
     return run_expert(layer, a, cap, accumulate, ws, reinterpret_cast<cudaStream_t>(s));
+}
+
+namespace {
+// the kernels read scales one fp32 at a time: 4-byte alignment suffices
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+bool fp8_scales_ok(const moe_weight_scales_t *sc, const float *x_scale) {
+    return sc != nullptr && sc->gate != nullptr && sc->up != nullptr && sc->down != nullptr && x_scale != nullptr &&
+           aligned4(sc->gate) && aligned4(sc->up) && aligned4(sc->down) && aligned4(x_scale);
+}
+}  // namespace
+
+moe_status_t moe_expert_op_perslot_fp8(const moe_layer_t *layer, const void *w_gate, const void *w_up,
+                                       const void *w_down, const moe_weight_scales_t *scales, const void *x,
+                                       const float *x_scale, const int32_t *ids, const float *gates, int32_t n,
+                                       int32_t accumulate, float *y, void *ws, size_t ws_bytes, moe_stream_t s) {
+    moe_status_t st = check_expert_common(layer, w_gate, w_up, w_down, x, gates, n, y, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (!is_fp8(layer)) return MOE_ERR_UNSUPPORTED;
+    if (ids == nullptr || !aligned16(ids) || !fp8_scales_ok(scales, x_scale)) return MOE_ERR_ARG;
+    ExpertArgs a = make_args(layer, w_gate, w_up, w_down, x, gates, n, y, ws, kModePerSlot);
+    a.ids = ids;
+    a.s_gate = scales->gate;
+    a.s_up = scales->up;
+    a.s_down = scales->down;
+    a.s_x = x_scale;
+    return run_expert(layer, a, n * layer->m, accumulate, ws, reinterpret_cast<cudaStream_t>(s));
+}
+
+moe_status_t moe_expert_op_dedup_fp8(const moe_layer_t *layer, const void *w_gate, const void *w_up,
+                                     const void *w_down, const moe_weight_scales_t *scales, const void *x,
+                                     const float *x_scale, const float *gates, int32_t n, const int32_t *num_distinct,
+                                     const int32_t *expert_list, const int32_t *expert_offsets,
+                                     const int32_t *slot_order, int32_t accumulate, float *y, void *ws,
+                                     size_t ws_bytes, moe_stream_t s) {
+    moe_status_t st = check_expert_common(layer, w_gate, w_up, w_down, x, gates, n, y, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (!is_fp8(layer)) return MOE_ERR_UNSUPPORTED;
+    const void *ptrs[] = {num_distinct, expert_list, expert_offsets, slot_order};
+    for (const void *p : ptrs)
+        if (p == nullptr || !aligned16(p)) return MOE_ERR_ARG;
+    if (!fp8_scales_ok(scales, x_scale)) return MOE_ERR_ARG;
+    ExpertArgs a = make_args(layer, w_gate, w_up, w_down, x, gates, n, y, ws, kModeDedup);
+    a.num_distinct = num_distinct;
+    a.expert_list = expert_list;
+    a.offsets = expert_offsets;
+    a.slot_order = slot_order;
+    a.s_gate = scales->gate;
+    a.s_up = scales->up;
+    a.s_down = scales->down;
+    a.s_x = x_scale;
+    const int cap = n * layer->m < layer->N ? n * layer->m : layer->N;
+    return run_expert(layer, a, cap, accumulate, ws, reinterpret_cast<cudaStream_t>(s));
+}
+
+moe_status_t moe_quantize_rows_e4m3(const void *src, int32_t src_dtype, int32_t rows, int32_t cols, uint8_t *q,
+                                    float *scale, moe_stream_t s) {
+    if (src_dtype != MOE_F32 && src_dtype != MOE_BF16) return MOE_ERR_ARG;
+    if (rows < 0 || cols < 1) return MOE_ERR_ARG;
+    if (rows == 0) return MOE_OK;
+    if (src == nullptr || q == nullptr || scale == nullptr) return MOE_ERR_ARG;
+    cudaError_t e = launch_quantize_rows(src, src_dtype, rows, cols, q, scale, reinterpret_cast<cudaStream_t>(s),
+                                         kUsePdl);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return cuda_status(e);
 }
 
 moe_status_t moe_pass_bytes(const moe_layer_t *layer, const int32_t *ids_host, int32_t n, moe_pass_bytes_t *out) {
@@ -208,12 +282,15 @@ moe_status_t moe_pass_bytes(const moe_layer_t *layer, const int32_t *ids_host, i
             ++U;
         }
     }
-    const uint64_t wsz = layer->w_dtype == MOE_BF16 ? 2u : 4u;
-    const uint64_t xsz = layer->x_dtype == MOE_BF16 ? 2u : 4u;
+    const uint64_t wsz = layer->w_dtype == MOE_BF16 ? 2u : (layer->w_dtype == MOE_E4M3 ? 1u : 4u);
+    const uint64_t xsz = layer->x_dtype == MOE_BF16 ? 2u : (layer->x_dtype == MOE_E4M3 ? 1u : 4u);
     out->expert_bytes = 3ull * static_cast<uint64_t>(layer->d) * static_cast<uint64_t>(layer->f) * wsz;
+    // an e4m3 expert also reads its fp32 row scales: 2f (gate, up) + d (down)
+    if (layer->w_dtype == MOE_E4M3) out->expert_bytes += 4ull * (2ull * layer->f + layer->d);
     out->slot_bytes = static_cast<uint64_t>(S) * out->expert_bytes;
     out->dedup_bytes = static_cast<uint64_t>(U) * out->expert_bytes;
-    out->act_bytes = static_cast<uint64_t>(n) * layer->d * xsz + static_cast<uint64_t>(n) * layer->d * 4ull;
+    out->act_bytes = static_cast<uint64_t>(n) * layer->d * xsz + static_cast<uint64_t>(n) * layer->d * 4ull +
+                     (layer->x_dtype == MOE_E4M3 ? 4ull * n : 0ull);
     out->n = n;
     out->m = layer->m;
     out->U = U;

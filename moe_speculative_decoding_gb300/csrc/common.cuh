@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda.h>          // CUtensorMap (type only; no driver symbol is linked)
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -170,6 +171,17 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// The same with e4m3 A and B (kind::f8f6f4, fp32 accumulators; K = 32 per instruction).
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on bar when every tcgen05.mma this thread issued so far has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -229,6 +241,28 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
            | (1u << 10)                               // B: bf16
            | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor of kind::f8f6f4 with e4m3 A and B (format code 0), fp32 D, both
+// K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+    return (1u << 4)                                  // D: fp32
+           | (0u << 7)                                // A: e4m3
+           | (0u << 10)                               // B: e4m3
+           | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// Round to the nearest e4m3 value, ties to even, saturating at +-448 (cvt.rn.satfinite).
+__device__ __forceinline__ uint8_t f32_to_e4m3(float v) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+    return static_cast<uint8_t>(r & 0xFFu);
+}
+
+// Named barrier over `count` threads (a multiple of 32) of the CTA; id 0 is __syncthreads'.
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ------------------------------------------------------------------ numerics

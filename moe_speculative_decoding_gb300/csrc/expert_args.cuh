@@ -28,6 +28,9 @@ struct ExpertArgs {
     const int32_t *slot_order;
     float *y;
     int32_t *err;
+    // e4m3 layers: fp32 scale of each weight row ([N, f], [N, f], [N, d]) and of each token
+    // ([n]); null for bf16
+    const float *s_gate, *s_up, *s_down, *s_x;
     int d, f, N, m, n, mode, w_dtype, x_dtype;
 };
 

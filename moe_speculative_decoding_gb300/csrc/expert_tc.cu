@@ -33,6 +33,13 @@
 //   MMAs, and add gate * (W_down h) into the fp32 output with atomics: the weighted
 //   combine and the reduction over f tiles are fused there.
 //
+// FP8 layers (e4m3 weights and x, one fp32 scale per weight row and per token) run the same
+// two kernels instantiated for kind::f8f6f4: a 128-byte row then holds 128 elements, so a
+// gate/up block is a 128-wide k slice and one down block covers the item's whole 128-wide
+// f span.  The gate/up epilogue applies the row and token scales to its partial sums; the
+// h formers quantize h per (token, 128-wide f span) with scale amax/448, and the down
+// epilogue applies that scale and the W_down row scale.
+//
 // Both kernels' shared memory fits one SM together (about 215 KB of 228 KB), so a down
 // CTA is resident beside a gate/up CTA and its first W_down stages are in flight before
 // the gate/up kernel ends.  Every wait is bounded (common.cuh); a time-out raises an abort
@@ -48,7 +55,6 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kBK = 64;                       // k elements per 128-byte row
 constexpr int kOB = 128;                      // d rows per down block
 constexpr int kNT = 16;                       // MMA N (token columns)
 constexpr uint32_t kWBytes = 16384;           // weight bytes of one block
@@ -61,8 +67,20 @@ constexpr int kDownBufs = 8;                  // TMEM ring of down-block accumul
 constexpr int kEpiBatch = 4;                  // down blocks per epilogue round
 constexpr uint32_t kGUTmemCols = 32;          // two 16-column accumulators
 constexpr uint32_t kDownTmemCols = 16 * kDownBufs;
-constexpr uint32_t kIdesc = idesc_bf16_f32(128, kNT);
 constexpr long long kDrainCycles = 400000000ll;   // about 0.2 s
+
+// Element type of a kernel instantiation: bf16 (kind::f16) or e4m3 (kind::f8f6f4).
+template <bool F8>
+struct Elt {
+    static constexpr int BK = F8 ? 128 : 64;   // k elements per 128-byte row of an operand tile
+    static constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(128, kNT) : idesc_bf16_f32(128, kNT);
+    // down blocks per unit: two 64-wide f tiles of bf16, or one 128-wide tile of e4m3
+    static constexpr int UNIT = F8 ? 1 : 2;
+    __device__ __forceinline__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
+        if constexpr (F8) tc_mma_f8(d, a, b, IDESC, acc);
+        else tc_mma_bf16(d, a, b, IDESC, acc);
+    }
+};
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
 // Shared memory of the gate/up kernel: stages, then barriers full[S], empty[S],
@@ -89,8 +107,9 @@ constexpr int kDnThreads = 256;               // + warps 6-7: the h formers
 constexpr uint32_t kDnH = kDownStages * kWBytes;
 constexpr uint32_t kHEntry = kDnSub * kHBytes;
 constexpr uint32_t kDnInfo = kDnH + kHRing * kHEntry;
-constexpr uint32_t kInfoBytes = 80;           // mask, then the 16 gates
-constexpr uint32_t kDnBars = kDnInfo + kHRing * kInfoBytes;
+constexpr uint32_t kInfoBytes = 144;          // mask, the 16 gates, the 16 h scales (FP8)
+constexpr uint32_t kDnScratch = kDnInfo + kHRing * kInfoBytes;   // [2][2 warps][16] h amax (FP8)
+constexpr uint32_t kDnBars = kDnScratch + 2 * 2 * kNT * 4;
 constexpr uint32_t kDnNumBars = 2 * kDownStages + 2 * kDownBufs + 2 * kHRing + 1;
 constexpr uint32_t kDnMisc = kDnBars + 8 * kDnNumBars;
 constexpr uint32_t kDnSmem = kDnMisc + 16 + 1024;
@@ -218,6 +237,7 @@ __device__ __forceinline__ void drain_copies(uint32_t bar_full, uint32_t cnt, in
 
 // ==================================================================== gate/up kernel
 
+template <bool F8>
 __global__ void __maxnreg__(kGUMaxRegs)
 expert_gu_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
                  const __grid_constant__ CUtensorMap tm_x, const ExpertArgs a, float *const part,
@@ -270,8 +290,9 @@ expert_gu_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     pdl_wait();
     pdl_trigger();
 
+    using E = Elt<F8>;
     const int T = a.f / kFTile;
-    const int KB = a.d / kBK;
+    const int KB = a.d / E::BK;
     const int G = num_groups(a);
     const Split sp{static_cast<long long>(G) * T * KB, gu_parts(G, T, gridDim.x)};
     const int c = blockIdx.x;
@@ -293,7 +314,7 @@ expert_gu_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                     ok = false;
                     break;
                 }
-                const int k0 = static_cast<int>(bb - static_cast<long long>(s.item) * KB) * kBK;
+                const int k0 = static_cast<int>(bb - static_cast<long long>(s.item) * KB) * E::BK;
                 if (elect_one()) {
                     const uint32_t dst = base + st * kGUStageBytes, fb = bar_full + 8u * st;
                     mbar_arrive_expect_tx(fb, kGUStageBytes);
@@ -335,9 +356,9 @@ expert_gu_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 const uint32_t sb = sa + kWBytes;
                 if (elect_one()) {
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k)
-                        tc_mma_bf16(d_tmem, desc_kmajor_sw128(sa + 32u * k), desc_kmajor_sw128(sb + 32u * k), kIdesc,
-                                    (bb != s.b0 || k != 0) ? 1u : 0u);
+                    for (int k = 0; k < 4; ++k)   // 32 bytes of K per instruction
+                        E::mma(d_tmem, desc_kmajor_sw128(sa + 32u * k), desc_kmajor_sw128(sb + 32u * k),
+                               (bb != s.b0 || k != 0) ? 1u : 0u);
                     tc_commit(bar_empty + 8u * st);
                     if (bb == s.b1 - 1) tc_commit(bar_acc_full + 8u * buf);
                 }
@@ -388,6 +409,14 @@ expert_gu_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             tc_fence_before();
             warp_arrive(bar_acc_empty + 8u * buf);
             if (slot < 0 || slot >= kMaxSpan) continue;   // not reachable with gu_parts' bound
+            if constexpr (F8) {
+                // integer-exact sums of codes back to values: weight-row scale times token scale
+                const int fr = s.e * a.f + s.tile * kFTile + (row & 63);
+                const float rs = row < 64 ? a.s_gate[fr] : a.s_up[fr];
+#pragma unroll
+                for (int t = 0; t < kNT; ++t)
+                    if ((gi.mask >> t) & 1u) v[t] *= rs * a.s_x[t];
+            }
 #pragma unroll
             for (int t = 0; t < kNT; ++t)
                 if ((gi.mask >> t) & 1u) part[part_index(gi.pos[t], T, s.tile, slot, row)] = v[t];
@@ -409,6 +438,7 @@ expert_gu_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
 // Registers: one SM sub-partition (a quarter of the 64K register file) holds up to two
 // warps of each kernel, so 2 * 32 * (down registers) + 2 * 32 * (gate/up registers) must stay
 // within 16384: with the gate/up kernel at 64, the down kernel gets at most 192.
+template <bool F8>
 __global__ void __maxnreg__(kDnMaxRegs)
 expert_down_kernel(const __grid_constant__ CUtensorMap tm_wd, const ExpertArgs a, const float *const part,
                    const int gu_grid) {
@@ -419,6 +449,7 @@ expert_down_kernel(const __grid_constant__ CUtensorMap tm_wd, const ExpertArgs a
     const uint32_t sh = base + kDnH;
     uint8_t *const h_ptr = base_ptr + kDnH;
     uint8_t *const info_ptr = base_ptr + kDnInfo;
+    float *const scratch = reinterpret_cast<float *>(base_ptr + kDnScratch);
     const uint32_t bar_full = base + kDnBars;
     const uint32_t bar_empty = bar_full + 8u * kDownStages;
     const uint32_t bar_acc_full = bar_empty + 8u * kDownStages;    // [kDownBufs]
@@ -471,11 +502,12 @@ expert_down_kernel(const __grid_constant__ CUtensorMap tm_wd, const ExpertArgs a
     // sub-tile s), s innermost, so the sub-tiles of one d block accumulate in one TMEM
     // accumulator: a unit.  The last item of a group has fewer real sub-tiles when T is
     // not a multiple of kDnSub; the others are skipped by every role alike.
+    using E = Elt<F8>;
     const int T = a.f / kFTile;
     const int T2 = (T + kDnSub - 1) / kDnSub;
-    const int KB = a.d / kBK;
+    const int KB = a.d / E::BK;
     const int OBS = a.d / kOB;
-    const int IB = OBS * kDnSub;   // blocks per item
+    const int IB = OBS * E::UNIT;   // blocks per item
     const int G = num_groups(a);
     const long long nblk = static_cast<long long>(G) * T2 * IB;
     const Split sp{nblk, static_cast<int>(nblk < 1 ? 1 : (nblk < gridDim.x ? nblk : gridDim.x))};
@@ -484,17 +516,19 @@ expert_down_kernel(const __grid_constant__ CUtensorMap tm_wd, const ExpertArgs a
     // the units of segment s: for (ob = ob_first; ob <= ob_last; ++ob) sub-tiles [s_lo, s_hi)
     struct Units {
         int r0, r1, nreal;
-        __device__ __forceinline__ int ob_first() const { return r0 / kDnSub; }
-        __device__ __forceinline__ int ob_last() const { return (r1 - 1) / kDnSub; }
-        __device__ __forceinline__ int s_lo(int ob) const { return max(0, r0 - ob * kDnSub); }
-        __device__ __forceinline__ int s_hi(int ob) const { return min(nreal, min(kDnSub, r1 - ob * kDnSub)); }
+        __device__ __forceinline__ int ob_first() const { return r0 / E::UNIT; }
+        __device__ __forceinline__ int ob_last() const { return (r1 - 1) / E::UNIT; }
+        __device__ __forceinline__ int s_lo(int ob) const { return max(0, r0 - ob * E::UNIT); }
+        __device__ __forceinline__ int s_hi(int ob) const { return min(nreal, min(E::UNIT, r1 - ob * E::UNIT)); }
     };
     auto units_of = [&](const Seg &sg) {
         Units u;
         const long long ib0 = static_cast<long long>(sg.item) * IB;
         u.r0 = static_cast<int>(sg.b0 - ib0);
         u.r1 = static_cast<int>(sg.b1 - ib0);
-        u.nreal = min(kDnSub, T - sg.tile * kDnSub);
+        // bf16: the item's 64-wide tiles present (the last item of a group may have one);
+        // e4m3: one block spans the item's 128 columns (f is a multiple of 128)
+        u.nreal = F8 ? 1 : min(kDnSub, T - sg.tile * kDnSub);
         return u;
     };
 
@@ -564,9 +598,9 @@ expert_down_kernel(const __grid_constant__ CUtensorMap tm_wd, const ExpertArgs a
                     const uint32_t sbs = sb + static_cast<uint32_t>(sub) * kHBytes;
                     if (elect_one()) {
 #pragma unroll
-                        for (int k = 0; k < kBK / 16; ++k)
-                            tc_mma_bf16(tmem + 16u * buf, desc_kmajor_sw128(sa + 32u * k),
-                                        desc_kmajor_sw128(sbs + 32u * k), kIdesc, (sub != s0 || k != 0) ? 1u : 0u);
+                        for (int k = 0; k < 4; ++k)   // 32 bytes of K per instruction
+                            E::mma(tmem + 16u * buf, desc_kmajor_sw128(sa + 32u * k), desc_kmajor_sw128(sbs + 32u * k),
+                                   (sub != s0 || k != 0) ? 1u : 0u);
                         tc_commit(bar_empty + 8u * st);
                         if (sub == s1 - 1) tc_commit(bar_acc_full + 8u * buf);
                     }
@@ -605,6 +639,10 @@ expert_down_kernel(const __grid_constant__ CUtensorMap tm_wd, const ExpertArgs a
             float gt[kNT];
 #pragma unroll
             for (int t = 0; t < kNT; ++t) gt[t] = __uint_as_float(rec[1 + t]);
+            if constexpr (F8) {
+#pragma unroll
+                for (int t = 0; t < kNT; ++t) gt[t] *= __uint_as_float(rec[17 + t]);   // h scale of the span
+            }
             warp_arrive(bar_h_empty + 8u * hb);
             // units in batches of up to kEpiBatch: their TMEM loads share one wait
             for (int ob = u.ob_first(); ok && ob <= u.ob_last();) {
@@ -641,10 +679,11 @@ expert_down_kernel(const __grid_constant__ CUtensorMap tm_wd, const ExpertArgs a
                 for (int j = 0; j < kEpiBatch; ++j) {
                     if (j >= nb) break;
                     const int o = obs[j] * kOB + row;
+                    const float ws = F8 ? a.s_down[static_cast<size_t>(sg.e) * a.d + o] : 1.0f;   // W_down row scale
 #pragma unroll
                     for (int t = 0; t < kNT; ++t)
                         if ((mask >> t) & 1u)
-                            atomicAdd(a.y + static_cast<size_t>(t) * a.d + o, gt[t] * __uint_as_float(r[j][t]));
+                            atomicAdd(a.y + static_cast<size_t>(t) * a.d + o, gt[t] * ws * __uint_as_float(r[j][t]));
                 }
             }
         }
@@ -657,6 +696,10 @@ expert_down_kernel(const __grid_constant__ CUtensorMap tm_wd, const ExpertArgs a
         const int i = static_cast<int>(threadIdx.x) - 192;   // 0..63
         const Split gsp{static_cast<long long>(G) * T * KB, gu_parts(G, T, gu_grid)};
         bool waited = false;
+        uint32_t hround = 0;        // e4m3: rounds of the amax exchange, alternating scratch halves
+        float hscale[kNT];          // e4m3: the run's h scale per token
+#pragma unroll
+        for (int t = 0; t < kNT; ++t) hscale[t] = 1.0f;
         uint32_t run = 0;
         for (long long b = lo; b < hi;) {
             const Seg sg = seg_at(a, b, hi, IB, T2);
@@ -698,19 +741,56 @@ expert_down_kernel(const __grid_constant__ CUtensorMap tm_wd, const ExpertArgs a
                         }
                     }
                 }
+                if constexpr (!F8) {
 #pragma unroll
-                for (int sub = 0; sub < kDnSub; ++sub) {
-                    if (sub >= nreal) break;
+                    for (int sub = 0; sub < kDnSub; ++sub) {
+                        if (sub >= nreal) break;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int t = 8 * h8 + j;
+                            if (!((gi.mask >> t) & 1u)) continue;
+                            const float hv = silu(pg[sub][j][0] + pg[sub][j][1] + pg[sub][j][2]) *
+                                             (pu[sub][j][0] + pu[sub][j][1] + pu[sub][j][2]);
+                            // 128-byte swizzle: row t of 128 bytes, 16-byte chunk (i/8) ^ (t%8)
+                            const uint32_t off = static_cast<uint32_t>(sub * kHBytes + (t >> 3) * 1024 + (t & 7) * 128 +
+                                                                       (((i >> 3) ^ (t & 7)) << 4) + (i & 7) * 2);
+                            *reinterpret_cast<__nv_bfloat16 *>(hp + off) = __float2bfloat16_rn(hv);
+                        }
+                    }
+                } else {
+                    // e4m3 h: each token's 128 values of the span share one scale, amax / 448,
+                    // reduced over the 64 threads (two warps) before any value is rounded
+                    float hv[kDnSub][8];
+#pragma unroll
+                    for (int sub = 0; sub < kDnSub; ++sub)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            hv[sub][j] = silu(pg[sub][j][0] + pg[sub][j][1] + pg[sub][j][2]) *
+                                         (pu[sub][j][0] + pu[sub][j][1] + pu[sub][j][2]);
+                    float *const sc = scratch + (hround & 1u) * (2 * kNT);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float mx = fmaxf(fabsf(hv[0][j]), fabsf(hv[1][j]));
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+                        if (lane == 0) sc[(warp - 6) * kNT + j] = mx;
+                    }
+                    named_barrier(1, 64);
+                    ++hround;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int t = 8 * h8 + j;
+                        const float amax = fmaxf(sc[j], sc[kNT + j]);
+                        const float hs = amax > 0.0f ? amax / 448.0f : 1.0f;
+                        hscale[t] = hs;
                         if (!((gi.mask >> t) & 1u)) continue;
-                        const float hv = silu(pg[sub][j][0] + pg[sub][j][1] + pg[sub][j][2]) *
-                                         (pu[sub][j][0] + pu[sub][j][1] + pu[sub][j][2]);
-                        // 128-byte swizzle: row t of 128 bytes, 16-byte chunk (i/8) ^ (t%8)
-                        const uint32_t off = static_cast<uint32_t>(sub * kHBytes + (t >> 3) * 1024 + (t & 7) * 128 +
-                                                                   (((i >> 3) ^ (t & 7)) << 4) + (i & 7) * 2);
-                        *reinterpret_cast<__nv_bfloat16 *>(hp + off) = __float2bfloat16_rn(hv);
+#pragma unroll
+                        for (int sub = 0; sub < kDnSub; ++sub) {
+                            const int fl = sub * 64 + i;   // column inside the 128-wide span
+                            const uint32_t off = static_cast<uint32_t>((t >> 3) * 1024 + (t & 7) * 128 +
+                                                                       (((fl >> 4) ^ (t & 7)) << 4) + (fl & 15));
+                            hp[off] = f32_to_e4m3(hv[sub][j] / hs);
+                        }
                     }
                 }
             }
@@ -719,6 +799,10 @@ expert_down_kernel(const __grid_constant__ CUtensorMap tm_wd, const ExpertArgs a
                 rec[0] = gi.mask;
 #pragma unroll
                 for (int t = 0; t < kNT; ++t) rec[1 + t] = __float_as_uint(gi.gt[t]);
+                if constexpr (F8) {
+#pragma unroll
+                    for (int t = 0; t < kNT; ++t) rec[17 + t] = __float_as_uint(hscale[t]);
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -757,72 +841,60 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [outer, inner] matrix, 128-byte swizzle.
-bool encode_2d(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+// 2-D tensor map over a row-major [outer, inner] matrix of 2-byte (bf16) or 1-byte (e4m3
+// codes) elements, 128-byte swizzle.  Coordinates and boxes are in elements.
+bool encode_2d(CUtensorMap *map, const void *ptr, bool bytes1, uint64_t inner, uint64_t outer, uint32_t box_inner,
                uint32_t box_outer) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * 2};
+    cuuint64_t strides[1] = {inner * (bytes1 ? 1 : 2)};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return fn(map, bytes1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+              const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 struct DeviceInfo {
     int sms = 0;
-    bool attr_set = false;
+    bool attr_set[2] = {false, false};
 };
 
 std::mutex g_info_mu;
 DeviceInfo g_info[64];
 
-}  // namespace
+template <bool F8>
+cudaError_t set_attributes() {
+    // the largest shared-memory carveout, so that a gate/up and a down CTA share an SM
+    cudaError_t err = cudaFuncSetAttribute(expert_gu_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGUSmem);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(expert_gu_kernel<F8>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   cudaSharedmemCarveoutMaxShared);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(expert_down_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDnSmem);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(expert_down_kernel<F8>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   cudaSharedmemCarveoutMaxShared);
+    return err;
+}
 
-bool expert_tc_supports(int d, int f) { return d % kOB == 0 && f % kFTile == 0 && d >= kOB && f >= kFTile; }
-
-cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, float *part, cudaStream_t s,
-                             bool pdl) {
-    if (!expert_tc_supports(a.d, a.f) || a.w_dtype != MOE_BF16 || a.x_dtype != MOE_BF16 || a.n > kNT ||
-        max_groups < 1)
-        return cudaErrorNotSupported;
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    int sms = 0;
-    {
-        std::lock_guard<std::mutex> lock(g_info_mu);
-        DeviceInfo &di = g_info[dev & 63];
-        if (!di.attr_set) {
-            err = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
-            // the largest shared-memory carveout, so that a gate/up and a down CTA share an SM
-            if (err == cudaSuccess)
-                err = cudaFuncSetAttribute(expert_gu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGUSmem);
-            if (err == cudaSuccess)
-                err = cudaFuncSetAttribute(expert_gu_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                           cudaSharedmemCarveoutMaxShared);
-            if (err == cudaSuccess)
-                err = cudaFuncSetAttribute(expert_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDnSmem);
-            if (err == cudaSuccess)
-                err = cudaFuncSetAttribute(expert_down_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                           cudaSharedmemCarveoutMaxShared);
-            if (err != cudaSuccess) return err;
-            di.attr_set = true;
-        }
-        sms = di.sms;
-    }
+template <bool F8>
+cudaError_t launch_pair(const ExpertArgs &a, int sms, int max_groups, bool zero_y, float *part, cudaStream_t s,
+                        bool pdl) {
+    using E = Elt<F8>;
     const long long T = a.f / kFTile, OBS = a.d / kOB;
     const int gu_grid = static_cast<int>(std::min<long long>(sms, 2ll * max_groups * T));
     const long long T2 = (T + kDnSub - 1) / kDnSub;
-    const int dn_grid = static_cast<int>(std::min<long long>(sms, static_cast<long long>(max_groups) * T2 * OBS * kDnSub));
+    const int dn_grid = static_cast<int>(std::min<long long>(sms, static_cast<long long>(max_groups) * T2 * OBS * E::UNIT));
 
     CUtensorMap tm_wg, tm_wu, tm_wd, tm_x;
     const uint64_t d = a.d, f = a.f, N = a.N;
-    if (!encode_2d(&tm_wg, a.w_gate, d, N * f, kBK, kFTile) || !encode_2d(&tm_wu, a.w_up, d, N * f, kBK, kFTile) ||
-        !encode_2d(&tm_wd, a.w_down, f, N * d, kBK, kOB) ||
-        !encode_2d(&tm_x, a.x, d, static_cast<uint64_t>(a.n), kBK, kNT))
+    if (!encode_2d(&tm_wg, a.w_gate, F8, d, N * f, E::BK, kFTile) ||
+        !encode_2d(&tm_wu, a.w_up, F8, d, N * f, E::BK, kFTile) ||
+        !encode_2d(&tm_wd, a.w_down, F8, f, N * d, E::BK, kOB) ||
+        !encode_2d(&tm_x, a.x, F8, d, static_cast<uint64_t>(a.n), E::BK, kNT))
         return cudaErrorInvalidValue;
 
     cudaLaunchAttribute attr[1];
@@ -833,15 +905,49 @@ cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, f
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-
     cfg.gridDim = dim3(static_cast<unsigned>(gu_grid));
     cfg.dynamicSmemBytes = kGUSmem;
-    err = cudaLaunchKernelEx(&cfg, expert_gu_kernel, tm_wg, tm_wu, tm_x, a, part, zero_y ? 1 : 0);
+    cudaError_t err = cudaLaunchKernelEx(&cfg, expert_gu_kernel<F8>, tm_wg, tm_wu, tm_x, a, part, zero_y ? 1 : 0);
     if (err != cudaSuccess) return err;
     cfg.gridDim = dim3(static_cast<unsigned>(dn_grid));
     cfg.blockDim = dim3(kDnThreads);
     cfg.dynamicSmemBytes = kDnSmem;
-    return cudaLaunchKernelEx(&cfg, expert_down_kernel, tm_wd, a, static_cast<const float *>(part), gu_grid);
+    return cudaLaunchKernelEx(&cfg, expert_down_kernel<F8>, tm_wd, a, static_cast<const float *>(part), gu_grid);
+}
+
+}  // namespace
+
+bool expert_tc_supports(int d, int f) { return d % kOB == 0 && f % kFTile == 0 && d >= kOB && f >= kFTile; }
+
+cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, float *part, cudaStream_t s,
+                             bool pdl) {
+    const bool f8 = a.w_dtype == MOE_E4M3 && a.x_dtype == MOE_E4M3;
+    const bool bf = a.w_dtype == MOE_BF16 && a.x_dtype == MOE_BF16;
+    if (!expert_tc_supports(a.d, a.f) || !(f8 || bf) || a.n > kNT || max_groups < 1) return cudaErrorNotSupported;
+    // e4m3: 128-element k slices and 128-wide f spans
+    if (f8 && (a.d % 128 != 0 || a.f % 128 != 0 || a.s_gate == nullptr || a.s_up == nullptr ||
+               a.s_down == nullptr || a.s_x == nullptr))
+        return cudaErrorNotSupported;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    int sms = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_info_mu);
+        DeviceInfo &di = g_info[dev & 63];
+        if (di.sms == 0) {
+            err = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+            if (err != cudaSuccess) return err;
+        }
+        if (!di.attr_set[f8 ? 1 : 0]) {
+            err = f8 ? set_attributes<true>() : set_attributes<false>();
+            if (err != cudaSuccess) return err;
+            di.attr_set[f8 ? 1 : 0] = true;
+        }
+        sms = di.sms;
+    }
+    return f8 ? launch_pair<true>(a, sms, max_groups, zero_y, part, s, pdl)
+              : launch_pair<false>(a, sms, max_groups, zero_y, part, s, pdl);
 }
 
 }  // namespace moe

@@ -290,11 +290,15 @@ int oracle_pass_bytes(int d, int f, int N, int m, int wdt, int xdt, const int32_
         if (!seen[ids[s]]) { seen[ids[s]] = 1; ++U; }
     }
     free(seen);
-    uint64_t w = 3ull * (uint64_t)d * (uint64_t)f * (uint64_t)dtype_size(wdt);
+    /* dtype 2 = e4m3: one byte per weight, plus the fp32 scale of each of the expert's
+     * 2f + d rows; the activations add their n fp32 token scales */
+    uint64_t wb = wdt == 2 ? 1u : (uint64_t)dtype_size(wdt);
+    uint64_t xb = xdt == 2 ? 1u : (uint64_t)dtype_size(xdt);
+    uint64_t w = 3ull * (uint64_t)d * (uint64_t)f * wb + (wdt == 2 ? 4ull * (2ull * f + d) : 0ull);
     out[0] = w;
     out[1] = (uint64_t)n * (uint64_t)m * w;
     out[2] = (uint64_t)U * w;
-    out[3] = (uint64_t)n * (uint64_t)d * (uint64_t)dtype_size(xdt) + (uint64_t)n * (uint64_t)d * 4ull;
+    out[3] = (uint64_t)n * (uint64_t)d * xb + (uint64_t)n * (uint64_t)d * 4ull + (xdt == 2 ? 4ull * n : 0ull);
     *U_out = U;
     *ubar = (n * m) > 0 ? (double)U / (double)(n * m) : 0.0;
     return 0;

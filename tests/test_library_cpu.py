@@ -21,7 +21,7 @@ def lib():
 def _declared_functions():
     text = open(os.path.join(ROOT, "include", "moe_verify.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(lib):
@@ -95,13 +95,13 @@ def test_noalloc_rejects_layers_beyond_its_scratch(lib):
 def test_pass_bytes_matches_oracle(lib, oracle_mod):
     rng = np.random.default_rng(40)
     for (d, f, N, m, dt) in [(2048, 768, 128, 8, "bf16"), (2048, 1408, 64, 6, "bf16"),
-                             (4096, 14336, 8, 2, "bf16"), (256, 512, 8, 2, "f32")]:
+                             (4096, 14336, 8, 2, "bf16"), (256, 512, 8, 2, "f32"), (2048, 768, 128, 8, "e4m3")]:
         L = api.make_layer(d, f, N, m, dt)
         for n in (1, 3, 8, 16):
             sets, _ = synth.routing_traces(1, n, N, m, float(rng.uniform(0, 1)), seed=int(rng.integers(1e9)))
             ids = sets[0]
             got = api.pass_bytes(L, ids)
-            code = 1 if dt == "bf16" else 0
+            code = {"bf16": 1, "f32": 0, "e4m3": 2}[dt]
             ref = oracle_mod.pass_bytes(d, f, N, ids, code, code)
             for k in ("expert_bytes", "slot_bytes", "dedup_bytes", "act_bytes", "U"):
                 assert got[k] == ref[k], k
@@ -232,3 +232,35 @@ def test_fit_op_times_matches_oracle(lib, oracle_mod):
                 assert g_ == pytest.approx(w_, rel=1e-7, abs=1e-22)
     with pytest.raises(api.MoeError):
         api.fit_op_times([2, 2, 2], [8, 8, 8], [1.0, 1.0, 1.0], m, b, "slot")   # rank 1
+
+
+def test_fp8_entry_points_validate(lib):
+    """e4m3 layers need the _fp8 calls (their scales); bf16 layers are refused there; NULL
+    scales or misaligned pointers are argument errors - all before any device work."""
+    P = ctypes.c_void_p
+    L8 = api.make_layer(2048, 768, 128, 8, "e4m3")
+    Lb = api.make_layer(2048, 768, 128, 8, "bf16")
+    fake = P(1 << 20)   # aligned, never dereferenced: validation fails first
+    ws = P(1 << 21)
+    wsb = lib.moe_workspace_bytes(ctypes.byref(L8), 16)
+    assert wsb == lib.moe_workspace_bytes(ctypes.byref(Lb), 16)
+    sc = api.WeightScales(fake, fake, fake)
+    args = (fake, fake, fake)
+    # plain call with an e4m3 layer
+    assert lib.moe_expert_op_perslot(ctypes.byref(L8), *args, fake, fake, fake, 4, 0, fake, ws, wsb, None) == 2
+    # fp8 call with a bf16 layer
+    assert lib.moe_expert_op_perslot_fp8(ctypes.byref(Lb), *args, ctypes.byref(sc), fake, fake, fake, fake, 4, 0,
+                                         fake, ws, wsb, None) == 2
+    # missing scales
+    assert lib.moe_expert_op_perslot_fp8(ctypes.byref(L8), *args, None, fake, fake, fake, fake, 4, 0, fake, ws,
+                                         wsb, None) == 1
+    bad = api.WeightScales(fake, None, fake)
+    assert lib.moe_expert_op_dedup_fp8(ctypes.byref(L8), *args, ctypes.byref(bad), fake, fake, fake, 4, fake, fake,
+                                       fake, fake, 0, fake, ws, wsb, None) == 1
+    # e4m3 needs d and f multiples of 128
+    L8b = api.make_layer(2048, 704, 128, 8, "e4m3")
+    assert lib.moe_expert_op_perslot_fp8(ctypes.byref(L8b), *args, ctypes.byref(sc), fake, fake, fake, fake, 4, 0,
+                                         fake, ws, wsb, None) == 2
+    assert lib.moe_quantize_rows_e4m3(None, 1, 4, 64, None, None, None) == 1
+    assert lib.moe_quantize_rows_e4m3(fake, 7, 4, 64, fake, fake, None) == 1
+    assert lib.moe_quantize_rows_e4m3(None, 1, 0, 64, None, None, None) == 0
