@@ -47,7 +47,7 @@ from moe_speculative_decoding_gb300.configs import BY_NAME, QWEN3_STACK  # noqa:
 
 METRIC = "MoE verify-pass expert-op µs and achieved HBM TB/s vs pass size n=1..16"
 UNIT = "TB/s"
-EXPERT_OP = "expert_gu_kernel+expert_down_kernel"
+EXPERT_OP = "expert_tc_kernel"
 A_GRID = [round(0.10 + 0.05 * i, 2) for i in range(18)]
 
 
@@ -192,8 +192,8 @@ def step_time_theory(n_values, Vs, Vd, Vw, bytes_slot, bytes_dedup, K):
 
 
 def fp8_leg(b: "StackBench", args, device, per_n_bf16):
-    """The same step with e4m3 experts (GB300's FP8 in place of the pages' quantized
-    experts): the stack quantized once, then per n and layer one activation quantization and
+    """The same step with e4m3 experts (GB300's FP8 in place of the quantized experts the
+    pages' engines run): the stack quantized once, then per n and layer one activation quantization and
     the FP8 expert operation, per-slot and dedup (the dedup grouping is the bf16 step's, the
     same kernel on the same ids; its time is added from that run).  Timed over the same
     windows after the bf16 measurement; value = FP8 expert bytes requested / time."""
@@ -313,7 +313,7 @@ def fp8_leg(b: "StackBench", args, device, per_n_bf16):
                 expert_bytes=int(api.pass_bytes(layer8, b.sets[0, :1])["expert_bytes"]),
                 quantize_s=round(t_quant, 2), per_n=rows, rel_rms_vs_bf16=round(worst, 5),
                 max_dev_dedup_vs_slot=round(worst_forms, 6),
-                launches_per_layer_form=3)
+                launches_per_layer_form=2)
 
 
 def fit_leg(wl, weights, device, reps: int = 7, windows: int = 8, n_max: int = 16):
@@ -448,9 +448,8 @@ class StackBench:
             st["bytes_slot"], st["bytes_dedup"] = bytes_slot, bytes_dedup
             self.per_n[n] = st
         self.graphs = {}
-        # per pass size: one route, 48 groupings, and two kernels (gate/up, down) per
-        # expert op in each form
-        self.launches_per_step = sum(1 + 5 * layers for _ in n_values)
+        # per pass size: one route, 48 groupings, and one kernel per expert op in each form
+        self.launches_per_step = sum(1 + 3 * layers for _ in n_values)
 
     # the four phases of one pass size
     def _route(self, st):
@@ -603,9 +602,8 @@ def run_ours(args, world, rank, local):
     else:
         theory = None
 
-    # roofline of the expert op (both forms; one launch = one layer's expert op, the
-    # gate/up and down kernels chained by programmatic dependent launch, which overlap:
-    # the down kernel's weight stream starts while the gate/up kernel still runs)
+    # roofline of the expert op (both forms; one launch = one layer's expert op, one
+    # persistent kernel streaming its gate/up and then its down weights)
     expert_s = sum(acc[(n, "slot")] + acc[(n, "dedup")] for n in n_values)
     launches = 2 * layers * len(n_values) * K
     peaks, peak_kind = measured_peaks()

@@ -96,9 +96,14 @@ moe_status_t run_expert(const moe_layer_t *L, const ExpertArgs &a, int max_group
                         cudaStream_t s) {
     cudaError_t e;
     if (uses_tc(L)) {
-        // the partial sums live after the workspace header; the gate/up kernel zeroes y
-        float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + kWorkspaceBytes);
-        e = launch_expert_tc(a, max_groups, !accumulate, part, s, kUsePdl);
+        // after the workspace header: the flags (sized for full passes, so that their place
+        // does not depend on n), then the partial sums; the kernel zeroes y
+        uint8_t *const w8 = static_cast<uint8_t *>(ws);
+        ExpertArgs at = a;
+        at.sync = &static_cast<DeviceWorkspace *>(ws)->sync[0];
+        at.flags = reinterpret_cast<uint32_t *>(w8 + kWorkspaceBytes);
+        float *part = reinterpret_cast<float *>(w8 + kWorkspaceBytes + expert_tc_flag_region(L->f, L->m));
+        e = launch_expert_tc(at, max_groups, !accumulate, part, s, kUsePdl);
     } else {
         e = cudaSuccess;
         if (!accumulate) e = cudaMemsetAsync(a.y, 0, sizeof(float) * static_cast<size_t>(a.n) * a.d, s);
@@ -131,8 +136,7 @@ const char *moe_status_str(moe_status_t status) {
 size_t moe_workspace_bytes(const moe_layer_t *layer, int32_t n_max) {
     if (check_layer(layer) != MOE_OK || n_max < 1 || !uses_tc(layer)) return kWorkspaceBytes;
     const int n = n_max < MOE_MAX_PASS_TOKENS ? n_max : MOE_MAX_PASS_TOKENS;
-    const size_t part = expert_tc_partial_bytes(layer->f, layer->m, n);
-    return kWorkspaceBytes + (part + 255) / 256 * 256;
+    return kWorkspaceBytes + expert_tc_flag_region(layer->f, layer->m) + round256(expert_tc_partial_bytes(layer->f, layer->m, n));
 }
 
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t s) {

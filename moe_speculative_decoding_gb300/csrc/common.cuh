@@ -17,7 +17,8 @@ namespace moe {
 // Device workspace layout.  Word 0 is the device error word (first error wins).
 struct DeviceWorkspace {
     int32_t error;
-    int32_t reserved[63];
+    uint32_t sync[2];   // tensor-core path: the epoch of its flags, and a CTA exit count
+    int32_t reserved[61];
 };
 constexpr size_t kWorkspaceBytes = sizeof(DeviceWorkspace);   // 256
 
@@ -79,6 +80,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity (try_wait may suspend the thread
+// for a while; this never does).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity.  Gives up when *abort becomes
 // non-zero (another role gave up) or after kWaitLimitCycles; on a time-out it raises the
 // abort flag and records MOE_ERR_DEVICE_TIMEOUT.  Returns true when the phase completed.
@@ -107,6 +122,47 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 __device__ __forceinline__ void warp_arrive(uint32_t bar) {
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// gpu-scope release store and acquire load of a 32-bit flag in global memory: a flag
+// written with st_release_gpu after a CTA's stores makes them visible to every thread that
+// reads the flag's value with ld_acquire_gpu.
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// gpu-scope atomic add with acquire and release semantics; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Warp-wide bounded wait until the flag of every lane holds `ticket` (lanes with p == nullptr
+// have none).  The same abort and time-limit rules as mbar_wait; the outcome is warp-uniform,
+// and every lane's later loads are ordered after the flags it waited for.
+__device__ __forceinline__ bool warp_wait_ticket(const uint32_t *p, uint32_t ticket, volatile int32_t *abort,
+                                                 int32_t *err) {
+    bool ok = p == nullptr || ld_acquire_gpu(p) == ticket;
+    const long long t0 = clock64();
+    while (!__all_sync(0xFFFFFFFFu, ok)) {
+        if (!ok) ok = ld_acquire_gpu(p) == ticket;
+        const bool late = clock64() - t0 > kWaitLimitCycles;
+        if (__any_sync(0xFFFFFFFFu, late || *abort != 0)) {
+            if (late) {
+                *abort = 1;
+                record_error(err, MOE_ERR_DEVICE_TIMEOUT);
+            }
+            return false;
+        }
+    }
+    __syncwarp();
+    return true;
 }
 
 // Bounded wait that ignores the abort flag (used to drain copies in flight on abort).

@@ -31,21 +31,36 @@ struct ExpertArgs {
     // e4m3 layers: fp32 scale of each weight row ([N, f], [N, f], [N, d]) and of each token
     // ([n]); null for bf16
     const float *s_gate, *s_up, *s_down, *s_x;
+    // tensor-core path: the workspace's epoch word and CTA exit count ([0], [1]), and its
+    // flags (expert_tc_flag_bytes)
+    uint32_t *sync;
+    uint32_t *flags;
     int d, f, N, m, n, mode, w_dtype, x_dtype;
 };
 
 cudaError_t launch_expert_simt(const ExpertArgs &a, int groups, cudaStream_t s, bool pdl);
 
-// Tensor-core path (bf16): a gate/up kernel and a down kernel.  The gate/up kernel's CTAs
-// share each (group, f tile) item's k blocks, at most kMaxSpan CTAs to an item, and hand
-// their fp32 partial sums to the down kernel through `part`: kMaxSpan * 128 floats per
-// (slot position, f tile), expert_tc_partial_bytes in all.  zero_y: y is overwritten
-// (zeroed by the gate/up kernel) rather than added to.  Returns cudaErrorNotSupported
-// when the shape is outside what it handles (the caller then reports MOE_ERR_UNSUPPORTED).
+// Tensor-core path (bf16 or e4m3): one kernel, one CTA per SM.  Its CTAs share each
+// (group, f tile) gate/up item's k blocks, at most kMaxSpan CTAs to an item, and hand their
+// fp32 partial sums to the CTAs that form h through `part`: kMaxSpan * 128 floats per (slot
+// position, f tile), expert_tc_partial_bytes in all, each share published by release flags
+// in `flags` (expert_tc_flag_bytes; zero when the workspace is initialised, never cleared
+// afterwards).  zero_y: y is overwritten (zeroed inside the kernel) rather than added to.
+// Returns cudaErrorNotSupported when the shape is outside what it handles (the caller then
+// reports MOE_ERR_UNSUPPORTED).
 constexpr int kMaxSpan = 3;
+constexpr int kMaxGrid = 256;   // CTAs of one call at most
 inline size_t expert_tc_partial_bytes(int f, int m, int n) {
     return static_cast<size_t>(n) * m * (f / kFTile) * kMaxSpan * 128 * sizeof(float);
 }
+inline size_t expert_tc_flag_bytes(int f, int m, int n) {
+    return (static_cast<size_t>(kMaxGrid) * 4 + static_cast<size_t>(n) * m * (f / kFTile) * kMaxSpan * 4) *
+           sizeof(uint32_t);
+}
+inline size_t round256(size_t bytes) { return (bytes + 255) / 256 * 256; }
+// The workspace's flag region: sized for full passes, so that its place and size do not
+// depend on the pass (the partial sums follow it).
+inline size_t expert_tc_flag_region(int f, int m) { return round256(expert_tc_flag_bytes(f, m, kMaxPassTokens)); }
 cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, float *part, cudaStream_t s,
                              bool pdl);
 bool expert_tc_supports(int d, int f);

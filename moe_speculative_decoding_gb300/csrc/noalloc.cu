@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "expert_args.cuh"
 
 namespace {
 
@@ -24,11 +25,14 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void *g_scratch_addr[kMaxDevices] = {};
+// the (f, m) of the last call's layer on each device: its flag region is in place
+int g_last_shape[kMaxDevices][2] = {};
 
 // Device address of the scratch on the current device.  In host code the array's name
 // only stands in for it, so the address is looked up once per device, with that device
-// current, and cached.
-cudaError_t scratch_address(void **out) {
+// current, and cached.  *shape_changed: the layer's (f, m) differs from the last call's on
+// this device (the tensor-core flags then sit elsewhere and must start from zero).
+cudaError_t scratch_address(const moe_layer_t *layer, void **out, bool *shape_changed) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -40,6 +44,9 @@ cudaError_t scratch_address(void **out) {
         if (e != cudaSuccess) return e;
         g_scratch_addr[dev] = p;
     }
+    *shape_changed = g_last_shape[dev][0] != layer->f || g_last_shape[dev][1] != layer->m;
+    g_last_shape[dev][0] = layer->f;
+    g_last_shape[dev][1] = layer->m;
     *out = g_scratch_addr[dev];
     return cudaSuccess;
 }
@@ -55,11 +62,17 @@ extern "C" moe_status_t moe_expert_op_perslot_noalloc(const moe_layer_t *layer, 
     if (moe_workspace_bytes(layer, n) > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
     if (status_out != nullptr && (reinterpret_cast<uintptr_t>(status_out) & 3u) != 0) return MOE_ERR_ARG;
     void *ws = nullptr;
-    if (scratch_address(&ws) != cudaSuccess) return MOE_ERR_CUDA;
+    bool shape_changed = false;
+    if (scratch_address(layer, &ws, &shape_changed) != cudaSuccess) return MOE_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
-    // the previous call's error word must not leak into this one; the partial sums are
-    // written before they are read and need no clearing
-    if (cudaMemsetAsync(ws, 0, moe::kWorkspaceBytes, st) != cudaSuccess) return MOE_ERR_CUDA;
+    // the previous call's error word must not leak into this one; the epoch word after it
+    // stays.  The flags start from zero when the layer's shape moved them; the partial sums
+    // are written before they are read and need no clearing.
+    if (cudaMemsetAsync(ws, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (shape_changed &&
+        cudaMemsetAsync(static_cast<uint8_t *>(ws) + moe::kWorkspaceBytes, 0,
+                        moe::expert_tc_flag_region(layer->f, layer->m), st) != cudaSuccess)
+        return MOE_ERR_CUDA;
     const moe_status_t r = moe_expert_op_perslot(layer, w_gate, w_up, w_down, x, ids, gates, n, accumulate, y, ws,
                                                  kNoAllocScratchBytes, s);
     if (r != MOE_OK) return r;

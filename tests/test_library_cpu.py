@@ -61,16 +61,20 @@ def test_argument_validation_before_any_launch(lib):
 
 
 def test_workspace_bytes(lib):
-    """256 header bytes, plus for the bf16 tensor-core path 3 CTA shares x 128 fp32 partial
-    sums per (slot, 64-row f tile): the gate/up kernel's hand-off to the down kernel."""
+    """256 header bytes, plus for the tensor-core path its flag region (4 words per CTA for
+    the zeroing of y, 256 CTAs, then 4 epilogue-warp flags per CTA share of a (slot, 64-row f
+    tile) gate/up item, 3 shares, sized for 16-token passes) and 3 CTA shares x 128 fp32
+    partial sums per (slot, 64-row f tile): the gate/up shares' hand-off to the h formers."""
+    r256 = lambda b: (b + 255) // 256 * 256
     for (d, f, N, m) in [(2048, 768, 128, 8), (2048, 1408, 64, 6), (4096, 14336, 8, 2), (256, 128, 8, 2)]:
         L = api.make_layer(d, f, N, m, "bf16")
+        flags = r256((256 * 4 + 16 * m * (f // 64) * 3 * 4) * 4)
         for n in (1, 5, 16):
             part = n * m * (f // 64) * 3 * 128 * 4
-            assert lib.moe_workspace_bytes(ctypes.byref(L), n) == 256 + (part + 255) // 256 * 256
+            assert lib.moe_workspace_bytes(ctypes.byref(L), n) == 256 + flags + r256(part)
         # passes cap at MOE_MAX_PASS_TOKENS
         assert lib.moe_workspace_bytes(ctypes.byref(L), 64) == lib.moe_workspace_bytes(ctypes.byref(L), 16)
-    assert lib.moe_workspace_bytes(ctypes.byref(api.make_layer(2048, 768, 128, 8)), 16) == 256 + 2359296
+    assert lib.moe_workspace_bytes(ctypes.byref(api.make_layer(2048, 768, 128, 8)), 16) == 256 + 77824 + 2359296
     # the SIMT kernel and fp32 layers keep only the header
     assert lib.moe_workspace_bytes(ctypes.byref(api.make_layer(256, 512, 8, 2, "f32")), 16) == 256
     assert lib.moe_workspace_bytes(ctypes.byref(api.make_layer(256, 512, 8, 2, "bf16", simt=True)), 16) == 256
