@@ -590,7 +590,8 @@ def run_ours(args, world, rank, local):
             saving_us=round(float(rep["saving"][i]) / K * 1e6, 2)))
     # best draft length: V(k) = expert time of a pass of k+1 tokens (all layers)
     kstar = {}
-    if n_values[0] == 1:
+    # the draft-length report needs the one-token pass and at least one longer one
+    if n_values[0] == 1 and len(n_values) > 1:
         Vs = [t / K for t in t_slot]
         Vd = [t_slot[0] / K] + [t / K for t in t_dedup[1:]]
         cross = rep["crossover"]
