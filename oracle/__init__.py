@@ -84,6 +84,10 @@ def _load():
         lib.oracle_err_decision_agrees.argtypes = [D, D, D]
         lib.oracle_err_kstar_separated.argtypes = [P, I, D, D]
         lib.oracle_err_speedup_interval.argtypes = [D, P, P]
+        lib.oracle_spec_accept.argtypes = [P, P, P, P, P, I, I, I, I, P, P]
+        lib.oracle_fx_draw.argtypes = [P, I, ctypes.c_float]
+        lib.oracle_fx_draw.restype = ctypes.c_int32
+        lib.oracle_union_cost.argtypes = [P, I, I, I, P, I, P, P, D, P, P, P, P, P]
         _lib = lib
     return _lib
 
@@ -403,3 +407,55 @@ def expert_op_token_fp8(wg, wu, wd, sg, su, sd, x, sx, ids, gates, t):
     if rc != 0:
         raise ValueError("oracle_expert_op_token_fp8: bad arguments")
     return y
+
+
+# ---------------------------------------------------------------- verify-side neighbours
+def spec_accept(draft, q, p, r, u, greedy: bool = False):
+    """One round of speculative sampling for B sequences ("Lossless but Not Free", §3.1,
+    Algorithm 1).  draft [B, K] int32, q [B, K, V] and p [B, K+1, V] float32, r [B, K] and
+    u [B] float32 uniforms.  Returns (n_accepted int32 [B], token int32 [B])."""
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    B, K1, V = p.shape
+    K = K1 - 1
+    draft = np.ascontiguousarray(np.asarray(draft, np.int32).reshape(B, K))
+    dummy = np.zeros(1, np.float32)
+    # the greedy rule reads neither q nor the draws
+    q = dummy if (q is None or K == 0) else np.ascontiguousarray(np.asarray(q, np.float32).reshape(B, K, V))
+    r = dummy if (r is None or K == 0) else np.ascontiguousarray(np.asarray(r, np.float32).reshape(B, K))
+    u = np.zeros(B, np.float32) if u is None else np.ascontiguousarray(np.asarray(u, np.float32).reshape(B))
+    if not greedy and K and (q is dummy or r is dummy):
+        raise ValueError("spec_accept: sampling needs q and r")
+    na = np.zeros(B, np.int32)
+    tok = np.zeros(B, np.int32)
+    rc = _load().oracle_spec_accept(_ptr(draft) if K else _ptr(np.zeros(1, np.int32)), _ptr(q), _ptr(p), _ptr(r),
+                                    _ptr(u), B, K, V, int(bool(greedy)), _ptr(na), _ptr(tok))
+    if rc != 0:
+        raise ValueError("oracle_spec_accept: bad arguments")
+    return na, tok
+
+
+def fx_draw(w, u: float) -> int:
+    """The fixed-point inverse-CDF draw alone (weights clamped to [0, 1]); -1 if all zero."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    return int(_load().oracle_fx_draw(_ptr(w), int(w.size), float(u)))
+
+
+def union_cost(bitmaps, subsets, pv, bcoef, beta: float):
+    """SpecFit §3.2 eqs (3)-(5): bitmaps uint64 [nodes+1, L, W] (node 0 the root), subsets
+    uint32 [S] node masks.  Returns dict(F, size, R, T, best)."""
+    bm = np.ascontiguousarray(bitmaps, dtype=np.uint64)
+    nodes1, L, W = bm.shape
+    sub = np.ascontiguousarray(subsets, dtype=np.uint32).reshape(-1)
+    pv = np.ascontiguousarray(pv, dtype=np.float64).reshape(nodes1 - 1) if nodes1 > 1 else np.zeros(1)
+    bc = np.ascontiguousarray(bcoef, dtype=np.float64)
+    S = sub.size
+    F = np.zeros(S, np.int32)
+    size = np.zeros(S, np.int32)
+    R = np.zeros(S, np.float64)
+    T = np.zeros(S, np.float64)
+    best = np.zeros(1, np.int32)
+    rc = _load().oracle_union_cost(_ptr(bm), nodes1 - 1, L, W, _ptr(sub) if S else _ptr(np.zeros(1, np.uint32)), S,
+                                   _ptr(pv), _ptr(bc), float(beta), _ptr(F), _ptr(size), _ptr(R), _ptr(T), _ptr(best))
+    if rc != 0:
+        raise ValueError("oracle_union_cost: bad arguments")
+    return dict(F=F, size=size, R=R, T=T, best=int(best[0]))

@@ -35,6 +35,12 @@
  *   oracle_quantize_rows_e4m3 the definition: scale = amax/448, codes round to nearest
  *   oracle_expert_op_token_fp8 the fp64 SwiGLU of the dequantized weights within the
  *                            rounding bound of the quantized h (2^-4 relative)
+ *   oracle_spec_accept       Proposition 1 of [Anatomy] by exact enumeration of draw grids
+ *                            (the emitted token is distributed as p), the one-hot / greedy
+ *                            equivalence, the expected yield (1 - a^{K+1})/(1 - a), hand cases
+ *   oracle_fx_draw           draw frequencies on a uniform u grid equal the weights' shares
+ *   oracle_union_cost        Python set unions per layer, monotone and submodular F,
+ *                            brute-force argmax of R/T
  */
 #include <math.h>
 #include <stdint.h>
@@ -751,5 +757,189 @@ int oracle_expert_op_token_fp8(int d, int f, int N, int m, const uint8_t *wg, co
     }
     free(h);
     free(hq);
+    return 0;
+}
+
+/* ================================================================ verify-side neighbours
+ *
+ * Speculative sampling: "Lossless but Not Free: An Empirical Anatomy of Speculative
+ * Decoding on Consumer Hardware", cited as [Anatomy]: §3.1 steps 3-4 (the accept test, eq.
+ * (1); the adjusted resample, eq. (2); the bonus token; Algorithm 1) and the greedy special
+ * case of §3.2.  The uniform draws r_i and u are inputs.  Single-precision arithmetic where
+ * the page fixes it ("sampling arithmetic is CPU float32"): the ratio p/q and its minimum
+ * with 1, and p - q.
+ *
+ * Reading for the draw from a distribution over V tokens: every weight w (clamped to [0, 1])
+ * becomes the integer W = floor(w * 2^46), Z = the exact sum of the W, and the drawn token is
+ * the smallest x whose running sum W(0) + ... + W(x) exceeds t = floor(Z * U / 2^24) with
+ * U = floor(u * 2^24).  Integer sums make the index independent of the summation order; each
+ * weight moves by less than 2^-46.
+ */
+
+static uint64_t fx_weight(float w)
+{
+    if (!(w > 0.0f)) return 0;                 /* zero, negative or NaN */
+    if (w >= 1.0f) return (uint64_t)1 << 46;
+    return (uint64_t)((double)w * 70368744177664.0);   /* exact product, truncated */
+}
+
+static uint32_t fx_u24(float u)
+{
+    if (!(u > 0.0f)) return 0;
+    if (u >= 1.0f) return (1u << 24) - 1u;
+    return (uint32_t)((double)u * 16777216.0);
+}
+
+/* The inverse-CDF draw above; -1 when every weight is zero. */
+static int32_t fx_draw(const uint64_t *W, int V, float u)
+{
+    uint64_t Z = 0;
+    for (int x = 0; x < V; ++x) Z += W[x];
+    if (Z == 0) return -1;
+    __extension__ unsigned __int128 prod = (unsigned __int128)Z * fx_u24(u);
+    const uint64_t t = (uint64_t)(prod >> 24);
+    uint64_t c = 0;
+    for (int x = 0; x < V; ++x) {
+        c += W[x];
+        if (c > t) return x;
+    }
+    return V - 1;   /* not reached: t < Z */
+}
+
+/* Lowest index of the largest value (a NaN never wins). */
+static int32_t argmax_row(const float *row, int V)
+{
+    int32_t best = 0;
+    for (int x = 1; x < V; ++x)
+        if (row[x] > row[best]) best = x;
+    return best;
+}
+
+/* The accept test of eq. (1): r < min(1, p(x)/q(x)) in single precision.  Reading for
+ * q(x) = 0 (a draft never samples such a token): accept iff p(x) > 0. */
+static int accept_draft(float px, float qx, float r)
+{
+    if (qx > 0.0f) {
+        const float ratio = px / qx;
+        const float thr = ratio < 1.0f ? ratio : 1.0f;
+        return r < thr;
+    }
+    return px > 0.0f;
+}
+
+/* One round of Algorithm 1 for each of B sequences.  draft [B, K] token ids x_1..x_K;
+ * q [B, K, V] the draft's distributions q_1..q_K; p [B, K+1, V] the target's p_1..p_{K+1};
+ * r [B, K] and u [B] uniform draws (ignored when greedy).  Out: n_acc[b] = a, the number of
+ * leading accepted drafts, and token[b] = the emitted token: a draw from p'_{a+1} of eq. (2)
+ * when a < K, the bonus draw from p_{K+1} when a = K.  Greedy (temperature 0): accept iff
+ * argmax p_i = x_i, and emit argmax p_{a+1}.  Readings: a draft id outside [0, V) is
+ * rejected; when the adjusted weights of eq. (2) are all zero the draw falls back to the
+ * target row p_{a+1} itself, and when that is all zero too, to its argmax. */
+int oracle_spec_accept(const int32_t *draft, const float *q, const float *p, const float *r, const float *u,
+                       int B, int K, int V, int greedy, int32_t *n_acc, int32_t *token)
+{
+    if (B < 0 || K < 0 || V < 1) return -1;
+    uint64_t *W = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)V);
+    if (W == NULL) return -1;
+    for (int b = 0; b < B; ++b) {
+        int a = 0;
+        for (; a < K; ++a) {
+            const int32_t x = draft[(size_t)b * K + a];
+            const float *pa = p + ((size_t)b * (K + 1) + a) * V;
+            if (x < 0 || x >= V) break;
+            if (greedy) {
+                if (argmax_row(pa, V) != x) break;
+            } else {
+                const float *qa = q + ((size_t)b * K + a) * V;
+                if (!accept_draft(pa[x], qa[x], r[(size_t)b * K + a])) break;
+            }
+        }
+        const float *prow = p + ((size_t)b * (K + 1) + a) * V;
+        int32_t y;
+        if (greedy) {
+            y = argmax_row(prow, V);
+        } else {
+            if (a < K) {
+                const float *qrow = q + ((size_t)b * K + a) * V;
+                for (int x = 0; x < V; ++x) {
+                    const float dlt = prow[x] - qrow[x];
+                    W[x] = fx_weight(dlt > 0.0f ? dlt : 0.0f);
+                }
+                y = fx_draw(W, V, u[b]);
+            } else {
+                y = -1;
+            }
+            if (y < 0) {
+                for (int x = 0; x < V; ++x) W[x] = fx_weight(prow[x]);
+                y = fx_draw(W, V, u[b]);
+            }
+            if (y < 0) y = argmax_row(prow, V);
+        }
+        n_acc[b] = a;
+        token[b] = y;
+    }
+    free(W);
+    return 0;
+}
+
+/* Exposed for the pins: the draw alone, on caller weights in [0, 1]. */
+int32_t oracle_fx_draw(const float *w, int V, float u)
+{
+    uint64_t *W = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(V > 0 ? V : 1));
+    if (W == NULL || V < 1) { free(W); return -2; }
+    for (int x = 0; x < V; ++x) W[x] = fx_weight(w[x]);
+    const int32_t y = fx_draw(W, V, u);
+    free(W);
+    return y;
+}
+
+/*
+ * Expert-union cost of a draft subtree: "SpecFit: Not All Draft Tokens Cost the Same in
+ * Offloaded MoE Inference", §3.2 eqs (3) and (4): F(S) = sum over layers l of
+ * |E_{l,s} u U_{v in S} E_{l,v}| with E_{l,v} the experts node v routes to in layer l (s the
+ * root), R(S) = 1 + sum_{v in S} p_v, T(S) = b_{|S|} + beta F(S).  bitmaps [nodes+1][L][W]
+ * 64-bit words, node 0 the root, expert e at bit e % 64 of word e / 64; subsets [count] node
+ * masks (bit v-1 for node v = 1..nodes <= 32); pv [nodes] (index v-1); bcoef [nodes+1].
+ * Out: F, size |S|, R, T per subset, and *best = the lowest index of the largest R/T ([SpecFit]
+ * eq. (5) over the given candidates).  R and T in double, p_v summed in node order.
+ */
+int oracle_union_cost(const uint64_t *bitmaps, int nodes, int L, int W, const uint32_t *subsets, int count,
+                      const double *pv, const double *bcoef, double beta, int32_t *F, int32_t *size, double *R,
+                      double *T, int32_t *best)
+{
+    if (nodes < 0 || nodes > 32 || L < 1 || W < 1 || count < 0) return -1;
+    int32_t bi = -1;
+    double bR = 0.0, bT = 1.0;
+    for (int c = 0; c < count; ++c) {
+        const uint32_t mask = subsets[c];
+        if (nodes < 32 && (mask >> nodes) != 0u) return -1;
+        int32_t f = 0;
+        for (int l = 0; l < L; ++l) {
+            for (int w = 0; w < W; ++w) {
+                uint64_t acc = bitmaps[((size_t)0 * L + l) * W + w];
+                for (int v = 1; v <= nodes; ++v)
+                    if ((mask >> (v - 1)) & 1u) acc |= bitmaps[((size_t)v * L + l) * W + w];
+                for (int bit = 0; bit < 64; ++bit) f += (int32_t)((acc >> bit) & 1u);
+            }
+        }
+        int32_t k = 0;
+        double rr = 1.0;
+        for (int v = 1; v <= nodes; ++v)
+            if ((mask >> (v - 1)) & 1u) {
+                ++k;
+                rr += pv[v - 1];
+            }
+        const double tt = bcoef[k] + beta * (double)f;
+        F[c] = f;
+        size[c] = k;
+        R[c] = rr;
+        T[c] = tt;
+        if (bi < 0 || rr / tt > bR / bT) {
+            bi = c;
+            bR = rr;
+            bT = tt;
+        }
+    }
+    *best = bi;
     return 0;
 }
