@@ -69,6 +69,7 @@ def parse():
                    help="only the chosen-id fits, on one freshly generated layer (prints their JSON)")
     p.add_argument("--fit-reps", type=int, default=7)
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-verify-side", action="store_true", help="skip the accept/reject and union-cost leg")
     return p.parse_args()
 
 
@@ -314,6 +315,93 @@ def fp8_leg(b: "StackBench", args, device, per_n_bf16):
                 quantize_s=round(t_quant, 2), per_n=rows, rel_rms_vs_bf16=round(worst, 5),
                 max_dev_dedup_vs_slot=round(worst_forms, 6),
                 launches_per_layer_form=2)
+
+
+def verify_side_leg(device, reps: int = 20, B: int = 16, K: int = 8, V: int = 151936, nodes: int = 18,
+                    layers: int = 48, N: int = 128, m: int = 8):
+    """The steps either side of the verification pass, timed on the device.
+    Speculative accept/reject ("Lossless but Not Free", §3.1, Algorithm 1) for B sequences of
+    K drafts over a V-token vocabulary (Qwen3's 151,936), sampling and greedy; algorithmic bytes
+    are the rows each call must read (p and q at the first rejection or p_{K+1}: sampling; the
+    K+1 target rows: greedy), and inputs rotate over sets whose total exceeds L2.  The
+    expert-union cost ([SpecFit] §3.2 eq. (4)) of every subset of an 18-node pool over 48
+    layers of 128 experts: an integer OR/popcount kernel, reported in subsets per second."""
+    g = torch.Generator(device=device)
+    g.manual_seed(synth.seed_for(0, stream=9001))
+    sets = 8
+    cases = []
+    for _ in range(sets):
+        zt = torch.randn((B, K + 1, V), generator=g, device=device) * 2.0
+        zd = 0.7 * zt[:, :K] + 0.3 * torch.randn((B, K, V), generator=g, device=device) * 2.0
+        p = torch.softmax(zt, -1).contiguous()
+        q = torch.softmax(zd, -1).contiguous()
+        draft = torch.multinomial(q.reshape(B * K, V), 1, generator=g).reshape(B, K).to(torch.int32).contiguous()
+        r = torch.rand((B, K), generator=g, device=device)
+        u = torch.rand((B,), generator=g, device=device)
+        cases.append((draft, q, p, r, u))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    out = {}
+    for greedy in (False, True):
+        # one call per input set, eagerly (the rows each call reads), then the same calls in a
+        # CUDA graph replayed back to back: device time per call without host launch gaps
+        outs = [(torch.empty(B, dtype=torch.int32, device=device), torch.empty(B, dtype=torch.int32, device=device))
+                for _ in range(sets)]
+        nbytes = 0
+        for c, (na, tok) in zip(cases, outs):
+            api.spec_accept(*c, greedy=greedy, n_accepted=na, token=tok)
+        torch.cuda.synchronize(device)
+        for na, _ in outs:
+            nbytes += B * (K + 1) * V * 4 if greedy else sum((2 if int(a) < K else 1) for a in na.cpu().tolist()) * V * 4
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for c, (na, tok) in zip(cases, outs):
+                api.spec_accept(*c, greedy=greedy, n_accepted=na, token=tok)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize(device)
+        ev[0].record()
+        for _ in range(reps):
+            graph.replay()
+        ev[1].record()
+        torch.cuda.synchronize(device)
+        t = ev[0].elapsed_time(ev[1]) * 1e-3 / (reps * sets)
+        per_call = nbytes / sets
+        out["greedy" if greedy else "sampling"] = dict(
+            us_per_call=round(t * 1e6, 2), gbps=round(per_call / t / 1e9, 1),
+            frac_of_hbm=round(per_call / t / 1e9 / measured_peaks()[0]["hbm_gbs"], 4),
+            bytes_per_call=int(per_call), mean_accepted=round(float(np.mean([o[0].float().mean().item() for o in outs])), 3))
+    # union cost of every subset of the pool
+    W = (N + 63) // 64
+    rng = np.random.default_rng(synth.seed_for(0, stream=9002))
+    bm = np.zeros((nodes + 1, layers, W), np.uint64)
+    for v in range(nodes + 1):
+        for l in range(layers):
+            for e in rng.choice(N, m, replace=False):
+                bm[v, l, e // 64] |= np.uint64(1) << np.uint64(e % 64)
+    bmt = torch.from_numpy(bm.view(np.int64)).to(device)
+    S = 1 << nodes
+    subs = torch.arange(S, dtype=torch.int64, device=device).to(torch.int32)
+    pv = torch.from_numpy(rng.random(nodes)).to(device)
+    bcoef = torch.from_numpy(np.sort(rng.random(nodes + 1))).to(device)
+    res = api.union_cost(bmt, subs, pv, bcoef, 0.4)
+    ws = torch.empty(int(api.lib().moe_union_cost_workspace_bytes(S)), dtype=torch.uint8, device=device)
+    for _ in range(3):
+        api.union_cost(bmt, subs, pv, bcoef, 0.4, out=res, ws=ws)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        api.union_cost(bmt, subs, pv, bcoef, 0.4, out=res, ws=ws)
+    graph.replay()
+    torch.cuda.synchronize(device)
+    ev[0].record()
+    for _ in range(reps):
+        graph.replay()
+    ev[1].record()
+    torch.cuda.synchronize(device)
+    t = ev[0].elapsed_time(ev[1]) * 1e-3 / reps
+    out["union_cost"] = dict(subsets=S, nodes=nodes, layers=layers, experts=N, us_per_call=round(t * 1e6, 2),
+                             subsets_per_s=round(S / t, 1), best=int(res["best"].item()), bound="alu")
+    out["config"] = dict(B=B, K=K, V=V, input_sets=sets, reps=reps, timing="CUDA-graph replays of one call per input set")
+    return out
 
 
 def fit_leg(wl, weights, device, reps: int = 7, windows: int = 8, n_max: int = 16):
@@ -636,6 +724,8 @@ def run_ours(args, world, rank, local):
         line["fp8"] = fp8_leg(b, args, device, per_n)
     if rank == 0 and not args.no_fit:
         line["fits"] = fit_leg(wl, b.weights[0], device, reps=args.fit_reps)
+    if rank == 0 and not args.no_verify_side:
+        line["verify_side"] = verify_side_leg(device)
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(b)
     if rank == 0:

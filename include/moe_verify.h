@@ -88,12 +88,16 @@ const char *moe_status_str(moe_status_t status);
 
 /*
  * Bytes of device workspace the expert-operation calls need for this layer and passes
- * of up to n_max tokens: 256 bytes holding the device error word and, for layers the bf16
- * tensor-core path runs, the fp32 gate/up partial sums its two kernels hand over,
- * 3 * 128 * 4 bytes per (slot, 64-row tile of f): 256 + n_max*m*(f/64)*1536 bytes
- * (2.4 MB for d = 2048, f = 768, top-8 at 16 tokens).  Zero it once with
- * moe_workspace_init before its first use; calls rewrite the partial sums before they
- * read them.  n_max above MOE_MAX_PASS_TOKENS counts as MOE_MAX_PASS_TOKENS.
+ * of up to n_max tokens: 256 bytes holding the device error word and, for layers the
+ * tensor-core kernel runs, a flag region (the per-call release flags with which the kernel's
+ * CTAs publish their gate/up shares and their zeroing of y; sized for 16-token passes:
+ * round256((1024 + 16*m*(f/64)*12) * 4) bytes) and the fp32 gate/up partial sums the CTAs
+ * hand to each other, 3 * 128 * 4 bytes per (slot, 64-row tile of f):
+ * 256 + flags + n_max*m*(f/64)*1536 bytes (2.44 MB for d = 2048, f = 768, top-8 at 16 tokens).
+ * Zero it once with moe_workspace_init before its first use; calls never clear the flags
+ * (each call publishes a new ticket) and rewrite the partial sums before they read them.  A
+ * workspace serves layers of one (f, m); zero it again before moving it to another shape.
+ * n_max above MOE_MAX_PASS_TOKENS counts as MOE_MAX_PASS_TOKENS.
  */
 size_t moe_workspace_bytes(const moe_layer_t *layer, int32_t n_max);
 
@@ -391,6 +395,52 @@ moe_status_t moe_fit_op_times(int32_t count, const int32_t *n, const int32_t *U,
  * (a moe_status_t value; MOE_OK if nothing was recorded) and clears it.
  */
 moe_status_t moe_last_device_error(void *ws, moe_stream_t s, int32_t *code);
+
+/* ---------------------------------------------------------------- verify-side neighbours */
+
+/*
+ * One round of speculative sampling for B sequences at once ("Lossless but Not Free: An
+ * Empirical Anatomy of Speculative Decoding on Consumer Hardware", §3.1 steps 3-4, eqs (1) and
+ * (2), Algorithm 1; §3.2 the greedy special case).  For each sequence b, drafts x_1..x_K are
+ * accepted while r_i < min(1, p_i(x_i)/q_i(x_i)) (single precision; q_i(x_i) = 0 accepts iff
+ * p_i(x_i) > 0; an id outside [0, V) is rejected); a = the number accepted.  The emitted token
+ * is drawn with u from p'_{a+1} ~ max(0, p_{a+1} - q_{a+1}) when a < K, from p_{K+1} (the
+ * bonus) when a = K; if those weights are all zero, from p_{a+1} itself, and if that is all
+ * zero, its argmax.  Greedy (temperature 0): accept iff argmax p_i = x_i, emit argmax p_{a+1}
+ * (lowest index among equal maxima); q, r and u are not read.
+ * The draw: W(x) = floor(w(x) * 2^46) of each weight clamped to [0, 1], Z = sum W, and the
+ * token is the smallest x with W(0) + ... + W(x) > floor(Z * floor(u * 2^24) / 2^24) (exact
+ * integer sums: the same token in any summation order).
+ *   draft [dev] int32 [B, K]; q [dev] fp32 [B, K, V]; p [dev] fp32 [B, K+1, V] (rows without
+ *   NaN); r [dev] fp32 [B, K], u [dev] fp32 [B] uniform draws in [0, 1);
+ *   n_accepted [dev] int32 [B] (a), token [dev] int32 [B].  All pointers 4-byte aligned.
+ * Supported: 0 <= K <= 31, 1 <= V <= 262144.  B == 0 enqueues nothing.  Asynchronous on s;
+ * no workspace.  Reads one row pair per sequence (p and q at the first rejection, or p_{K+1})
+ * in sampling mode, the K+1 target rows in greedy mode.
+ */
+moe_status_t moe_spec_accept(const int32_t *draft, const float *q, const float *p, const float *r, const float *u,
+                             int32_t B, int32_t K, int32_t V, int32_t greedy, int32_t *n_accepted, int32_t *token,
+                             moe_stream_t s);
+
+/*
+ * Expert-union cost of candidate draft subtrees ("SpecFit: Not All Draft Tokens Cost the Same
+ * in Offloaded MoE Inference", §3.2 eqs (3)-(5)).  A pool of `nodes` draft nodes (<= 32) plus
+ * the root s; for each candidate subset S (a node mask, bit v-1 for node v; bits beyond the
+ * pool are ignored):
+ *   F(S) = sum_{l < L} |E_{l,s} u U_{v in S} E_{l,v}|,  size = |S|,
+ *   R(S) = 1 + sum_{v in S} p_v (summed in node order),  T(S) = bcoef[|S|] + beta * F(S),
+ * and *best = the lowest index of the largest R/T (-1 when count == 0).  R, T in double.
+ *   bitmaps [dev] uint64 [nodes+1][L][W] (node 0 the root; expert e at bit e % 64 of word e / 64;
+ *   (nodes+1)*L*W*8 <= 200 KB); subsets [dev] uint32 [count]; pv [dev] double [nodes];
+ *   bcoef [dev] double [nodes+1]; F, size [dev] int32 [count]; R, T [dev] double [count];
+ *   best [dev] int32 [1]; ws [dev] of moe_union_cost_workspace_bytes(count) bytes (16-byte
+ *   aligned).  Asynchronous on s.
+ */
+size_t moe_union_cost_workspace_bytes(int32_t count);
+moe_status_t moe_union_cost(const uint64_t *bitmaps, int32_t nodes, int32_t L, int32_t W, const uint32_t *subsets,
+                            int32_t count, const double *pv, const double *bcoef, double beta, int32_t *F,
+                            int32_t *size, double *R, double *T, int32_t *best, void *ws, size_t ws_bytes,
+                            moe_stream_t s);
 
 #ifdef __cplusplus
 }

@@ -67,7 +67,8 @@ EXPORTED = ("moe_abi_version", "moe_status_str", "moe_workspace_bytes", "moe_wor
             "moe_best_draft_length", "moe_last_device_error", "moe_expert_op_perslot_noalloc",
             "moe_staircase", "moe_speedup", "moe_reuse_threshold", "moe_reuse_threshold_bytes",
             "moe_error_bounds", "moe_kstar_separated", "moe_fit_op_times", "moe_expert_op_perslot_fp8",
-            "moe_expert_op_dedup_fp8", "moe_quantize_rows_e4m3")
+            "moe_expert_op_dedup_fp8", "moe_quantize_rows_e4m3", "moe_spec_accept",
+            "moe_union_cost_workspace_bytes", "moe_union_cost")
 
 _lib = None
 
@@ -114,6 +115,9 @@ def lib():
         "moe_expert_op_dedup_fp8": ([LP, P, P, P, ctypes.POINTER(WeightScales), P, P, P, I32, P, P, P, P, I32, P,
                                      P, SZ, P], I32),
         "moe_quantize_rows_e4m3": ([P, I32, I32, I32, P, P, P], I32),
+        "moe_spec_accept": ([P, P, P, P, P, I32, I32, I32, I32, P, P, P], I32),
+        "moe_union_cost_workspace_bytes": ([I32], SZ),
+        "moe_union_cost": ([P, I32, I32, I32, P, I32, P, P, D, P, P, P, P, P, P, SZ, P], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -414,3 +418,48 @@ def expert_op_dedup_fp8(layer: Layer, weights, scales, xq: torch.Tensor, x_scale
                                          int(bool(accumulate)), yp, ctypes.c_void_p(ws.data_ptr()),
                                          ws.numel(), _stream(xq.device)), "moe_expert_op_dedup_fp8")
     return y
+
+
+# ---------------------------------------------------------------- verify-side neighbours
+def spec_accept(draft, q, p, r, u, greedy: bool = False, n_accepted=None, token=None):
+    """One round of speculative sampling for B sequences ("Lossless but Not Free", §3.1,
+    Algorithm 1) on the device.  draft int32 [B, K], q fp32 [B, K, V], p fp32 [B, K+1, V],
+    r fp32 [B, K], u fp32 [B] (q, r, u may be None when greedy).  Returns (n_accepted, token),
+    int32 [B] each."""
+    B, K1, V = p.shape
+    K = K1 - 1
+    dev = p.device
+    if n_accepted is None:
+        n_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    if token is None:
+        token = torch.empty(B, dtype=torch.int32, device=dev)
+    dptr = lambda t, name, dt: None if t is None else _dev(t, name, dt)
+    _check(lib().moe_spec_accept(dptr(draft, "draft", torch.int32) if K else None, dptr(q, "q", torch.float32),
+                                 _dev(p, "p", torch.float32), dptr(r, "r", torch.float32), dptr(u, "u", torch.float32),
+                                 B, K, V, int(bool(greedy)), _dev(n_accepted, "n_accepted", torch.int32),
+                                 _dev(token, "token", torch.int32), _stream(dev)), "moe_spec_accept")
+    return n_accepted, token
+
+
+def union_cost(bitmaps, subsets, pv, bcoef, beta: float, out=None, ws=None):
+    """SpecFit §3.2 eqs (3)-(5) on the device: bitmaps uint64-as-int64 [nodes+1, L, W], subsets
+    int32/uint32 bits [S], pv float64 [nodes], bcoef float64 [nodes+1].  Returns dict(F, size,
+    R, T, best) of device tensors."""
+    nodes1, L, W = bitmaps.shape
+    S = subsets.numel()
+    dev = bitmaps.device
+    if out is None:
+        out = dict(F=torch.empty(S, dtype=torch.int32, device=dev), size=torch.empty(S, dtype=torch.int32, device=dev),
+                   R=torch.empty(S, dtype=torch.float64, device=dev), T=torch.empty(S, dtype=torch.float64, device=dev),
+                   best=torch.empty(1, dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = torch.empty(int(lib().moe_union_cost_workspace_bytes(S)), dtype=torch.uint8, device=dev)
+    _check(lib().moe_union_cost(_dev(bitmaps, "bitmaps", torch.int64), nodes1 - 1, L, W,
+                                _dev(subsets, "subsets", torch.int32), S,
+                                _dev(pv, "pv", torch.float64) if nodes1 > 1 else None,
+                                _dev(bcoef, "bcoef", torch.float64), float(beta),
+                                _dev(out["F"], "F", torch.int32), _dev(out["size"], "size", torch.int32),
+                                _dev(out["R"], "R", torch.float64), _dev(out["T"], "T", torch.float64),
+                                _dev(out["best"], "best", torch.int32), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                _stream(dev)), "moe_union_cost")
+    return out

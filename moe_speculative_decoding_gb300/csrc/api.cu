@@ -12,6 +12,7 @@
 
 #include "common.cuh"
 #include "expert_args.cuh"
+#include "spec_args.cuh"
 
 namespace moe {
 cudaError_t launch_route_topm(const float *logits, int n, int N, int m, int renorm, int32_t *ids, float *gates,
@@ -526,6 +527,79 @@ moe_status_t moe_fit_op_times(int32_t count, const int32_t *n, const int32_t *U,
     }
     for (int j = 0; j < 3; ++j) coef[j] = x[j] / scale[j];
     return MOE_OK;
+}
+
+moe_status_t moe_spec_accept(const int32_t *draft, const float *q, const float *p, const float *r, const float *u,
+                             int32_t B, int32_t K, int32_t V, int32_t greedy, int32_t *n_accepted, int32_t *token,
+                             moe_stream_t s) {
+    if (B < 0 || K < 0 || V < 1) return MOE_ERR_ARG;
+    if (K > kMaxSpecK || V > kMaxSpecV) return MOE_ERR_UNSUPPORTED;
+    if (B == 0) return MOE_OK;
+    auto al4 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; };
+    if (p == nullptr || n_accepted == nullptr || token == nullptr || !al4(p) || !al4(n_accepted) || !al4(token))
+        return MOE_ERR_ARG;
+    if (K > 0 && (draft == nullptr || !al4(draft))) return MOE_ERR_ARG;
+    if (!greedy) {
+        if (u == nullptr || !al4(u)) return MOE_ERR_ARG;
+        if (K > 0 && (q == nullptr || r == nullptr || !al4(q) || !al4(r))) return MOE_ERR_ARG;
+    }
+    SpecArgs a;
+    a.draft = draft;
+    a.q = q;
+    a.p = p;
+    a.r = r;
+    a.u = u;
+    a.n_acc = n_accepted;
+    a.token = token;
+    a.B = B;
+    a.K = K;
+    a.V = V;
+    a.greedy = greedy ? 1 : 0;
+    a.seg = spec_segment(V);
+    a.vec = (V % 4 == 0 && aligned16(p) && (greedy || K == 0 || aligned16(q))) ? 1 : 0;
+    cudaError_t e = launch_spec_accept(a, reinterpret_cast<cudaStream_t>(s), kUsePdl);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return cuda_status(e);
+}
+
+size_t moe_union_cost_workspace_bytes(int32_t count) {
+    return count < 1 ? 16 : round256(union_cost_scratch_bytes(count));
+}
+
+moe_status_t moe_union_cost(const uint64_t *bitmaps, int32_t nodes, int32_t L, int32_t W, const uint32_t *subsets,
+                            int32_t count, const double *pv, const double *bcoef, double beta, int32_t *F,
+                            int32_t *size, double *R, double *T, int32_t *best, void *ws, size_t ws_bytes,
+                            moe_stream_t s) {
+    if (nodes < 0 || L < 1 || W < 1 || count < 0) return MOE_ERR_ARG;
+    if (nodes > 32 || static_cast<size_t>(nodes + 1) * L * W * sizeof(uint64_t) > kMaxUnionSmem)
+        return MOE_ERR_UNSUPPORTED;
+    if (best == nullptr || (reinterpret_cast<uintptr_t>(best) & 3u) != 0) return MOE_ERR_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+    if (count == 0) return cuda_status(cudaMemsetAsync(best, 0xFF, sizeof(int32_t), st));
+    auto al = [](const void *ptr, uintptr_t m) { return ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & m) == 0; };
+    if (!al(bitmaps, 7) || !al(subsets, 3) || !al(bcoef, 7) || !al(F, 3) || !al(size, 3) || !al(R, 7) || !al(T, 7))
+        return MOE_ERR_ARG;
+    if (nodes > 0 && !al(pv, 7)) return MOE_ERR_ARG;
+    if (ws == nullptr || !aligned16(ws)) return MOE_ERR_ARG;
+    if (ws_bytes < moe_union_cost_workspace_bytes(count)) return MOE_ERR_WORKSPACE;
+    UnionArgs a;
+    a.bitmaps = bitmaps;
+    a.subsets = subsets;
+    a.pv = pv;
+    a.bcoef = bcoef;
+    a.beta = beta;
+    a.F = F;
+    a.size = size;
+    a.R = R;
+    a.T = T;
+    a.best = best;
+    a.nodes = nodes;
+    a.L = L;
+    a.W = W;
+    a.count = count;
+    cudaError_t e = launch_union_cost(a, ws, st, kUsePdl);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return cuda_status(e);
 }
 
 moe_status_t moe_last_device_error(void *ws, moe_stream_t s, int32_t *code) {

@@ -899,7 +899,8 @@ int32_t oracle_fx_draw(const float *w, int V, float u)
  * |E_{l,s} u U_{v in S} E_{l,v}| with E_{l,v} the experts node v routes to in layer l (s the
  * root), R(S) = 1 + sum_{v in S} p_v, T(S) = b_{|S|} + beta F(S).  bitmaps [nodes+1][L][W]
  * 64-bit words, node 0 the root, expert e at bit e % 64 of word e / 64; subsets [count] node
- * masks (bit v-1 for node v = 1..nodes <= 32); pv [nodes] (index v-1); bcoef [nodes+1].
+ * masks (bit v-1 for node v = 1..nodes <= 32; higher bits ignored); pv [nodes] (index v-1);
+ * bcoef [nodes+1].
  * Out: F, size |S|, R, T per subset, and *best = the lowest index of the largest R/T ([SpecFit]
  * eq. (5) over the given candidates).  R and T in double, p_v summed in node order.
  */
@@ -911,8 +912,8 @@ int oracle_union_cost(const uint64_t *bitmaps, int nodes, int L, int W, const ui
     int32_t bi = -1;
     double bR = 0.0, bT = 1.0;
     for (int c = 0; c < count; ++c) {
-        const uint32_t mask = subsets[c];
-        if (nodes < 32 && (mask >> nodes) != 0u) return -1;
+        /* bits beyond the pool name no node and are ignored */
+        const uint32_t mask = subsets[c] & (nodes >= 32 ? 0xFFFFFFFFu : ((1u << nodes) - 1u));
         int32_t f = 0;
         for (int l = 0; l < L; ++l) {
             for (int w = 0; w < W; ++w) {

@@ -268,3 +268,28 @@ def test_fp8_entry_points_validate(lib):
     assert lib.moe_quantize_rows_e4m3(None, 1, 4, 64, None, None, None) == 1
     assert lib.moe_quantize_rows_e4m3(fake, 7, 4, 64, fake, fake, None) == 1
     assert lib.moe_quantize_rows_e4m3(None, 1, 0, 64, None, None, None) == 0
+
+
+def test_verify_side_calls_validate_on_the_host(lib):
+    """moe_spec_accept and moe_union_cost reject bad sizes and pointers before any device work."""
+    P = ctypes.c_void_p
+    good = P(64)
+    # K above one warp's walk, V above the fixed-point range
+    assert lib.moe_spec_accept(good, good, good, good, good, 4, 32, 1000, 0, good, good, None) == 2
+    assert lib.moe_spec_accept(good, good, good, good, good, 4, 8, 262145, 0, good, good, None) == 2
+    assert lib.moe_spec_accept(good, good, good, good, good, -1, 8, 1000, 0, good, good, None) == 1
+    assert lib.moe_spec_accept(good, good, good, good, good, 4, 8, 0, 0, good, good, None) == 1
+    assert lib.moe_spec_accept(None, None, None, None, None, 0, 8, 1000, 0, None, None, None) == 0   # B == 0
+    assert lib.moe_spec_accept(good, good, None, good, good, 4, 8, 1000, 0, good, good, None) == 1   # p
+    assert lib.moe_spec_accept(good, None, good, good, good, 4, 8, 1000, 0, good, good, None) == 1   # q
+    assert lib.moe_spec_accept(good, good, good, good, P(66), 4, 8, 1000, 0, good, good, None) == 1  # u align
+    # union cost: pool size, shared-memory bound, workspace
+    assert lib.moe_union_cost(good, 33, 4, 2, good, 10, good, good, 0.5, good, good, good, good, good, good,
+                              4096, None) == 2
+    assert lib.moe_union_cost(good, 32, 1000, 4, good, 10, good, good, 0.5, good, good, good, good, good, good,
+                              4096, None) == 2
+    assert lib.moe_union_cost(good, 8, 4, 2, good, 10, good, good, 0.5, good, good, good, good, good, None,
+                              4096, None) == 1
+    assert lib.moe_union_cost(good, 8, 4, 2, good, 1000, good, good, 0.5, good, good, good, good, good, good,
+                              16, None) == 4
+    assert lib.moe_union_cost_workspace_bytes(1000) >= 4 * 12

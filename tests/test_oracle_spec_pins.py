@@ -203,6 +203,9 @@ def test_union_cost_against_set_unions_and_properties():
     ratio = out["R"] / out["T"]
     assert out["best"] == int(np.argmax(ratio))
     assert out["F"][0] == L * m            # the root alone
+    # bits beyond the pool name no node
+    extra = oracle.union_cost(bm, np.array([subsets[5] | (1 << nodes) | (1 << 31)], np.uint32), pv, bcoef, beta)
+    assert extra["F"][0] == out["F"][5] and extra["size"][0] == out["size"][5]
     # monotone, submodular
     for _ in range(200):
         a = int(rng.integers(0, 1 << nodes))
