@@ -70,6 +70,8 @@ def parse():
     p.add_argument("--fit-reps", type=int, default=7)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-verify-side", action="store_true", help="skip the accept/reject and union-cost leg")
+    p.add_argument("--verify-side-only", action="store_true", help="run only the accept/reject and union-cost leg")
+    p.add_argument("--verify-reps", type=int, default=20)
     return p.parse_args()
 
 
@@ -725,7 +727,7 @@ def run_ours(args, world, rank, local):
     if rank == 0 and not args.no_fit:
         line["fits"] = fit_leg(wl, b.weights[0], device, reps=args.fit_reps)
     if rank == 0 and not args.no_verify_side:
-        line["verify_side"] = verify_side_leg(device)
+        line["verify_side"] = verify_side_leg(device, reps=args.verify_reps)
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(b)
     if rank == 0:
@@ -857,6 +859,10 @@ def main():
         device = torch.device("cuda", 0)
         w = synth.expert_weights(wl.N, wl.f, wl.d, torch.bfloat16, synth.seed_for(wl.index, layer=0), device=device)
         print(json.dumps(dict(workload=wl.name, fits=fit_leg(wl, w, device, reps=args.fit_reps))), flush=True)
+        return
+    if args.verify_side_only:
+        mbuild.build()
+        print(json.dumps(dict(verify_side=verify_side_leg(torch.device("cuda", 0), reps=args.verify_reps))), flush=True)
         return
     world, rank, local = dist_setup(args)
     run_ours(args, world, rank, local)
