@@ -197,8 +197,7 @@ def step_time_theory(n_values, Vs, Vd, Vw, bytes_slot, bytes_dedup, K):
 def fp8_leg(b: "StackBench", args, device, per_n_bf16):
     """The same step with e4m3 experts (GB300's FP8 in place of the quantized experts the
     pages' engines run): the stack quantized once, then per n and layer one activation quantization and
-    the FP8 expert operation, per-slot and dedup (the dedup grouping is the bf16 step's, the
-    same kernel on the same ids; its time is added from that run).  Timed over the same
+    the FP8 expert operation, per-slot and dedup (one launch each; the dedup launch groups the slots).  Timed over the same
     windows after the bf16 measurement; value = FP8 expert bytes requested / time."""
     wl, L = b.wl, b.L
     layer8 = api.make_layer(wl.d, wl.f, wl.N, wl.m, "e4m3")
@@ -231,8 +230,8 @@ def fp8_leg(b: "StackBench", args, device, per_n_bf16):
             api._check(api.lib().moe_quantize_rows_e4m3(ctypes.c_void_p(st["x"].data_ptr()), api.MOE_BF16, n, wl.d,
                                                         ctypes.c_void_p(xq.data_ptr()), ctypes.c_void_p(sx.data_ptr()),
                                                         api._stream(device)), "moe_quantize_rows_e4m3")
-            api.expert_op_dedup_fp8(layer8, w8[l][0], w8[l][1], xq, sx, st["gates"][l * n:(l + 1) * n],
-                                    st["groups"][l], y=bf["yd"][l], accumulate=True, ws=ws8)
+            api.expert_op_dedup_ids_fp8(layer8, w8[l][0], w8[l][1], xq, sx, st["ids"][l * n:(l + 1) * n],
+                                        st["gates"][l * n:(l + 1) * n], y=bf["yd"][l], accumulate=True, ws=ws8)
 
     graphs = {}
     for n in b.n_values:
@@ -255,7 +254,6 @@ def fp8_leg(b: "StackBench", args, device, per_n_bf16):
         for n in b.n_values:
             b.stage(n, w)
             b._run(n, "route")
-            b._run(n, "group")
             bufs[n]["ys"].zero_()
             bufs[n]["yd"].zero_()
             if ev is not None:
@@ -287,13 +285,12 @@ def fp8_leg(b: "StackBench", args, device, per_n_bf16):
                 pb = api.pass_bytes(layer8, b.sets[l, w * n:(w + 1) * n])
                 bs += pb["slot_bytes"]
                 bd += pb["dedup_bytes"]
-        tg = bf16[n]["us_dedup_group"] * 1e-6 * K
         tot_b += bs + bd
-        tot_t += ts + td + tg
-        rows.append(dict(n=n, us_slot=round(ts / K * 1e6, 2), us_dedup=round((td + tg) / K * 1e6, 2),
-                         tbps_slot=round(bs / ts / 1e12, 3), tbps_dedup_kernel=round(bd / td / 1e12, 3),
+        tot_t += ts + td
+        rows.append(dict(n=n, us_slot=round(ts / K * 1e6, 2), us_dedup=round(td / K * 1e6, 2),
+                         tbps_slot=round(bs / ts / 1e12, 3), tbps_dedup=round(bd / td / 1e12, 3),
                          speedup_slot=round(bf16[n]["us_slot"] / (ts / K * 1e6), 3),
-                         speedup_dedup=round(bf16[n]["us_dedup"] / ((td + tg) / K * 1e6), 3)))
+                         speedup_dedup=round(bf16[n]["us_dedup"] / (td / K * 1e6), 3)))
     # outputs against the bf16 per-slot pass of the same (last) window: quantization error only;
     # the FP8 forms against each other: accumulation order only
     worst, worst_forms = 0.0, 0.0
@@ -303,7 +300,6 @@ def fp8_leg(b: "StackBench", args, device, per_n_bf16):
         b._run(n, "slot")
         bufs[n]["ys"].zero_()
         bufs[n]["yd"].zero_()
-        b._run(n, "group")
         run(n, "slot8")
         run(n, "dedup8")
         torch.cuda.synchronize(device)
@@ -538,8 +534,8 @@ class StackBench:
             st["bytes_slot"], st["bytes_dedup"] = bytes_slot, bytes_dedup
             self.per_n[n] = st
         self.graphs = {}
-        # per pass size: one route, 48 groupings, and one kernel per expert op in each form
-        self.launches_per_step = sum(1 + 3 * layers for _ in n_values)
+        # per pass size: one route and one kernel per expert op in each form
+        self.launches_per_step = sum(1 + 2 * layers for _ in n_values)
 
     # the four phases of one pass size
     def _route(self, st):
@@ -555,9 +551,10 @@ class StackBench:
             api.group_slots(st["ids"][l * n:(l + 1) * n], self.wl.N, out=st["groups"][l], ws=self.ws)
 
     def _dedup(self, st, n):
+        # the deduplicating form in one launch per layer: the kernel builds the pass's grouping
         for l in range(self.L):
-            api.expert_op_dedup(self.layer, self.weights[l], st["x"], st["gates"][l * n:(l + 1) * n],
-                                st["groups"][l], y=st["y_dedup"][l], accumulate=True, ws=self.ws)
+            api.expert_op_dedup_ids(self.layer, self.weights[l], st["x"], st["ids"][l * n:(l + 1) * n],
+                                    st["gates"][l * n:(l + 1) * n], y=st["y_dedup"][l], accumulate=True, ws=self.ws)
 
     def capture(self):
         phases = ("route", "slot", "group", "dedup")
@@ -592,12 +589,16 @@ class StackBench:
         st["y_slot"].zero_()
         st["y_dedup"].zero_()
 
+    # the timed phases of a pass size; "group" (the standalone counting sort) runs only for the
+    # checks: the deduplicating launch groups the slots itself
+    TIMED = ("route", "slot", "dedup")
+
     def step(self, w, events=None):
         for n in self.n_values:
             self.stage(n, w)
             if events is not None:
                 events[(n, "start")].record()
-            for ph in ("route", "slot", "group", "dedup"):
+            for ph in self.TIMED:
                 self._run(n, ph)
                 if events is not None:
                     events[(n, ph)].record()
@@ -632,7 +633,7 @@ def run_ours(args, world, rank, local):
         b.step(w)
     torch.cuda.synchronize(device)
 
-    phases = ("route", "slot", "group", "dedup")
+    phases = b.TIMED
     events = [{(n, k): torch.cuda.Event(enable_timing=True) for n in n_values for k in ("start",) + phases}
               for _ in range(args.steps)]
     acc = {(n, ph): 0.0 for n in n_values for ph in phases}
@@ -664,7 +665,7 @@ def run_ours(args, world, rank, local):
     total_bytes = sum(bytes_slot.values()) + sum(bytes_dedup.values())
     value = world * total_bytes / total_s / 1e12
     t_slot = [acc[(n, "slot")] for n in n_values]
-    t_dedup = [acc[(n, "group")] + acc[(n, "dedup")] for n in n_values]
+    t_dedup = [acc[(n, "dedup")] for n in n_values]
     rep = api.bandwidth_report(n_values[0], [bytes_slot[n] for n in n_values],
                                [bytes_dedup[n] for n in n_values], t_slot, t_dedup)
     K = args.steps
@@ -673,7 +674,7 @@ def run_ours(args, world, rank, local):
         per_n.append(dict(
             n=n,
             us_slot=round(t_slot[i] / K * 1e6, 2), us_dedup=round(t_dedup[i] / K * 1e6, 2),
-            us_dedup_group=round(acc[(n, "group")] / K * 1e6, 2), us_route=round(acc[(n, "route")] / K * 1e6, 2),
+            us_route=round(acc[(n, "route")] / K * 1e6, 2),
             tbps_slot=round(rep["beta_slot"][i] / 1e12, 3), tbps_dedup=round(rep["beta_dedup"][i] / 1e12, 3),
             tbps_dedup_kernel=round(bytes_dedup[n] / acc[(n, "dedup")] / 1e12, 3),
             ubar=round(float(rep["ubar"][i]), 4), r=round(float(rep["r"][i]), 4),
@@ -753,7 +754,7 @@ def e2e_run(b: StackBench, args, world, device, total_bytes_per_step):
             st["x"].copy_(hs["x"][w], non_blocking=True)
             st["y_slot"].zero_()
             st["y_dedup"].zero_()
-            for ph in ("route", "slot", "group", "dedup"):
+            for ph in b.TIMED:
                 b._run(n, ph)
             hs["y_slot"].copy_(st["y_slot"], non_blocking=True)
             hs["y_dedup"].copy_(st["y_dedup"], non_blocking=True)

@@ -181,6 +181,21 @@ moe_status_t moe_expert_op_dedup(const moe_layer_t *layer, const void *w_gate, c
                                  moe_stream_t s);
 
 /*
+ * The deduplicating form from the slots' ids in one launch: the same result as
+ * moe_group_slots followed by moe_expert_op_dedup ([Lan] §1: each distinct expert of the pass
+ * read once, its tokens batched), with the grouping (the counting sort on expert id) built
+ * inside the kernel, once per CTA in shared memory, instead of by a launch of its own.
+ *   Arguments as moe_expert_op_perslot (ids [dev] int32 [n*m] as there).  Ids outside
+ *   [0, N) are left out of every group and set MOE_ERR_BAD_ID in the workspace.
+ * Supported: the layers the tensor-core kernel runs (bf16, d a multiple of 128), n*m <= 256;
+ * otherwise MOE_ERR_UNSUPPORTED (use the two calls).
+ */
+moe_status_t moe_expert_op_dedup_ids(const moe_layer_t *layer, const void *w_gate, const void *w_up,
+                                     const void *w_down, const void *x, const int32_t *ids, const float *gates,
+                                     int32_t n, int32_t accumulate, float *y, void *ws, size_t ws_bytes,
+                                     moe_stream_t s);
+
+/*
  * The per-slot expert operation without a caller workspace.  The paper has no
  * counterpart: this is a service to callers that cannot allocate device memory -- code
  * running under a memory manager that owns every device byte (a serving framework's
@@ -235,6 +250,12 @@ moe_status_t moe_expert_op_dedup_fp8(const moe_layer_t *layer, const void *w_gat
                                      const int32_t *expert_list, const int32_t *expert_offsets,
                                      const int32_t *slot_order, int32_t accumulate, float *y, void *ws,
                                      size_t ws_bytes, moe_stream_t s);
+
+/* The e4m3 form of moe_expert_op_dedup_ids (scales as moe_expert_op_perslot_fp8). */
+moe_status_t moe_expert_op_dedup_ids_fp8(const moe_layer_t *layer, const void *w_gate, const void *w_up,
+                                         const void *w_down, const moe_weight_scales_t *scales, const void *x,
+                                         const float *x_scale, const int32_t *ids, const float *gates, int32_t n,
+                                         int32_t accumulate, float *y, void *ws, size_t ws_bytes, moe_stream_t s);
 
 /*
  * Per-row quantization to e4m3 on the device (the operand format of the _fp8 calls): for each

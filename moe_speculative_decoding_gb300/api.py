@@ -68,7 +68,8 @@ EXPORTED = ("moe_abi_version", "moe_status_str", "moe_workspace_bytes", "moe_wor
             "moe_staircase", "moe_speedup", "moe_reuse_threshold", "moe_reuse_threshold_bytes",
             "moe_error_bounds", "moe_kstar_separated", "moe_fit_op_times", "moe_expert_op_perslot_fp8",
             "moe_expert_op_dedup_fp8", "moe_quantize_rows_e4m3", "moe_spec_accept",
-            "moe_union_cost_workspace_bytes", "moe_union_cost")
+            "moe_union_cost_workspace_bytes", "moe_union_cost", "moe_expert_op_dedup_ids",
+            "moe_expert_op_dedup_ids_fp8")
 
 _lib = None
 
@@ -116,6 +117,9 @@ def lib():
                                      P, SZ, P], I32),
         "moe_quantize_rows_e4m3": ([P, I32, I32, I32, P, P, P], I32),
         "moe_spec_accept": ([P, P, P, P, P, I32, I32, I32, I32, P, P, P], I32),
+        "moe_expert_op_dedup_ids": ([LP, P, P, P, P, P, P, I32, I32, P, P, SZ, P], I32),
+        "moe_expert_op_dedup_ids_fp8": ([LP, P, P, P, ctypes.POINTER(WeightScales), P, P, P, P, I32, I32, P, P, SZ, P],
+                                        I32),
         "moe_union_cost_workspace_bytes": ([I32], SZ),
         "moe_union_cost": ([P, I32, I32, I32, P, I32, P, P, D, P, P, P, P, P, P, SZ, P], I32),
     }
@@ -237,6 +241,21 @@ def expert_op_perslot(layer: Layer, weights, x: torch.Tensor, ids: torch.Tensor,
                                        _dev(gates, "gates", torch.float32, (n, layer.m)), n,
                                        int(bool(accumulate)), yp, ctypes.c_void_p(ws.data_ptr()),
                                        ws.numel(), _stream(x.device)), "moe_expert_op_perslot")
+    return y
+
+
+def expert_op_dedup_ids(layer: Layer, weights, x: torch.Tensor, ids: torch.Tensor, gates: torch.Tensor,
+                        y=None, accumulate: bool = False, ws=None):
+    """The deduplicating form from ids in one launch (the grouping built inside the kernel)."""
+    n = x.shape[0]
+    ws = ws if ws is not None else workspace(layer, n, x.device)
+    y, yp = _y(layer, x, y)
+    _check(lib().moe_expert_op_dedup_ids(ctypes.byref(layer), *_weights(layer, weights),
+                                         _dev(x, "x", layer.torch_dtype, (n, layer.d)),
+                                         _dev(ids, "ids", torch.int32, (n, layer.m)),
+                                         _dev(gates, "gates", torch.float32, (n, layer.m)), n,
+                                         int(bool(accumulate)), yp, ctypes.c_void_p(ws.data_ptr()),
+                                         ws.numel(), _stream(x.device)), "moe_expert_op_dedup_ids")
     return y
 
 
@@ -398,6 +417,22 @@ def expert_op_perslot_fp8(layer: Layer, weights, scales, xq: torch.Tensor, x_sca
                                            _dev(gates, "gates", torch.float32, (n, layer.m)), n,
                                            int(bool(accumulate)), yp, ctypes.c_void_p(ws.data_ptr()),
                                            ws.numel(), _stream(xq.device)), "moe_expert_op_perslot_fp8")
+    return y
+
+
+def expert_op_dedup_ids_fp8(layer: Layer, weights, scales, xq: torch.Tensor, x_scale: torch.Tensor, ids: torch.Tensor,
+                            gates: torch.Tensor, y=None, accumulate: bool = False, ws=None):
+    n = xq.shape[0]
+    ws = ws if ws is not None else workspace(layer, n, xq.device)
+    y, yp = _y(layer, xq, y)
+    sc = _scales(layer, scales)
+    _check(lib().moe_expert_op_dedup_ids_fp8(ctypes.byref(layer), *_weights(layer, weights), ctypes.byref(sc),
+                                             _dev(xq, "x", torch.uint8, (n, layer.d)),
+                                             _dev(x_scale, "x_scale", torch.float32, (n,)),
+                                             _dev(ids, "ids", torch.int32, (n, layer.m)),
+                                             _dev(gates, "gates", torch.float32, (n, layer.m)), n,
+                                             int(bool(accumulate)), yp, ctypes.c_void_p(ws.data_ptr()),
+                                             ws.numel(), _stream(xq.device)), "moe_expert_op_dedup_ids_fp8")
     return y
 
 

@@ -207,6 +207,20 @@ moe_status_t moe_expert_op_dedup(const moe_layer_t *layer, const void *w_gate, c
     return run_expert(layer, a, cap, accumulate, ws, reinterpret_cast<cudaStream_t>(s));
 }
 
+moe_status_t moe_expert_op_dedup_ids(const moe_layer_t *layer, const void *w_gate, const void *w_up,
+                                     const void *w_down, const void *x, const int32_t *ids, const float *gates,
+                                     int32_t n, int32_t accumulate, float *y, void *ws, size_t ws_bytes,
+                                     moe_stream_t s) {
+    moe_status_t st = check_expert_common(layer, w_gate, w_up, w_down, x, gates, n, y, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (is_fp8(layer) || !uses_tc(layer) || n * layer->m > kMaxFusedSlots) return MOE_ERR_UNSUPPORTED;
+    if (ids == nullptr || !aligned16(ids)) return MOE_ERR_ARG;
+    ExpertArgs a = make_args(layer, w_gate, w_up, w_down, x, gates, n, y, ws, kModeDedupIds);
+    a.ids = ids;
+    const int cap = n * layer->m < layer->N ? n * layer->m : layer->N;
+    return run_expert(layer, a, cap, accumulate, ws, reinterpret_cast<cudaStream_t>(s));
+}
+
 namespace {
 // the kernels read scales one fp32 at a time: 4-byte alignment suffices
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -232,6 +246,24 @@ moe_status_t moe_expert_op_perslot_fp8(const moe_layer_t *layer, const void *w_g
     a.s_down = scales->down;
     a.s_x = x_scale;
     return run_expert(layer, a, n * layer->m, accumulate, ws, reinterpret_cast<cudaStream_t>(s));
+}
+
+moe_status_t moe_expert_op_dedup_ids_fp8(const moe_layer_t *layer, const void *w_gate, const void *w_up,
+                                         const void *w_down, const moe_weight_scales_t *scales, const void *x,
+                                         const float *x_scale, const int32_t *ids, const float *gates, int32_t n,
+                                         int32_t accumulate, float *y, void *ws, size_t ws_bytes, moe_stream_t s) {
+    moe_status_t st = check_expert_common(layer, w_gate, w_up, w_down, x, gates, n, y, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (!is_fp8(layer) || n * layer->m > kMaxFusedSlots) return MOE_ERR_UNSUPPORTED;
+    if (ids == nullptr || !aligned16(ids) || !fp8_scales_ok(scales, x_scale)) return MOE_ERR_ARG;
+    ExpertArgs a = make_args(layer, w_gate, w_up, w_down, x, gates, n, y, ws, kModeDedupIds);
+    a.ids = ids;
+    a.s_gate = scales->gate;
+    a.s_up = scales->up;
+    a.s_down = scales->down;
+    a.s_x = x_scale;
+    const int cap = n * layer->m < layer->N ? n * layer->m : layer->N;
+    return run_expert(layer, a, cap, accumulate, ws, reinterpret_cast<cudaStream_t>(s));
 }
 
 moe_status_t moe_expert_op_dedup_fp8(const moe_layer_t *layer, const void *w_gate, const void *w_up,

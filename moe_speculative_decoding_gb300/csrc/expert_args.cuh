@@ -10,7 +10,10 @@ namespace moe {
 constexpr int kMaxPassTokens = MOE_MAX_PASS_TOKENS;   // tokens per pass (MMA N = 16)
 constexpr int kFTile = 64;                             // rows of f per work item
 
-enum : int { kModePerSlot = 0, kModeDedup = 1 };
+// kModeDedupIds: the deduplicating form from the slots' ids, the grouping built inside the
+// tensor-core kernel (at most kMaxFusedSlots slots).
+enum : int { kModePerSlot = 0, kModeDedup = 1, kModeDedupIds = 2 };
+constexpr int kMaxFusedSlots = 256;
 
 // One call of the expert operation.  Per-slot form: group g is slot g (expert ids[g],
 // token g / m).  Deduplicating form: group g is expert_list[g] with the slots

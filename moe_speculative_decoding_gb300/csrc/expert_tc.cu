@@ -82,7 +82,12 @@ constexpr uint32_t kSxOff = kInfoOff + kHRing * kInfoBytes;
 constexpr uint32_t kBarOff = kSxOff + 4 * kNT * 4;
 constexpr int kNumBars = 2 * kStages + 4 + 2 * kDownBufs + 2 * kHRing + 1;
 constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
-constexpr uint32_t kSmem = kMiscOff + 16 + 1024;   // + alignment slack of the base
+// the grouping of the deduplicating form from ids: expert list, offsets, slot order, the count,
+// two scan scratch rows, then the per-expert counts (N <= 1024)
+constexpr uint32_t kGrpOff = kMiscOff + 16;
+constexpr uint32_t kGrpWords = 3 * kMaxFusedSlots + 1 + 1 + 16;
+constexpr uint32_t kCntOff = kGrpOff + ((kGrpWords * 4 + 15) & ~15u);
+constexpr uint32_t kSmem = kCntOff + 1024 * 4 + 1024;   // + alignment slack of the base
 static_assert(kSlotBytes % 1024 == 0 && kHOff % 1024 == 0 && kHEntry % 1024 == 0, "128-byte swizzle atoms");
 static_assert(kBarOff % 8 == 0, "mbarrier alignment");
 static_assert(kSmem <= 232448, "shared memory of one CTA");
@@ -236,6 +241,89 @@ __device__ __forceinline__ uint32_t call_ticket(const uint32_t *sync) {
 // The k-th token (ascending) of a token mask, or a value >= 16 when it has fewer.
 __device__ __forceinline__ uint32_t nth_token(uint32_t mask, int k) { return __fns(mask, 0u, k + 1); }
 
+// The grouping of the deduplicating form (the counting sort of moe_group_slots): experts in
+// ascending order with their slot offsets, slots of an expert in ascending order; ids outside
+// [0, N) are left out of every group.  All threads of the CTA take part.
+__device__ void build_grouping(const ExpertArgs &a, int32_t *lst, int32_t *off, int32_t *ord, int32_t *cnt,
+                               int32_t *g_out, int32_t *scan) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int N = a.N, S = a.n * a.m;
+    for (int i = tid; i < N; i += kThreads) cnt[i] = 0;
+    __syncthreads();
+    bool bad = false;
+    for (int s = tid; s < S; s += kThreads) {
+        const int e = a.ids[s];
+        if (e >= 0 && e < N) atomicAdd(&cnt[e], 1);
+        else bad = true;
+    }
+    if (__syncthreads_or(bad) && tid == 0 && blockIdx.x == 0) record_error(a.err, MOE_ERR_BAD_ID);
+    // thread tid owns bins [4 tid, 4 tid + 4): exclusive scans of the slot counts and of the
+    // non-empty bins over the CTA
+    int c[4], cs = 0, ne = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int b = 4 * tid + j;
+        c[j] = b < N ? cnt[b] : 0;
+        cs += c[j];
+        ne += c[j] > 0 ? 1 : 0;
+    }
+    int is = cs, in = ne;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int us = __shfl_up_sync(kFull, is, o), un = __shfl_up_sync(kFull, in, o);
+        if (lane >= o) {
+            is += us;
+            in += un;
+        }
+    }
+    if (lane == 31) {
+        scan[warp] = is;
+        scan[8 + warp] = in;
+    }
+    __syncthreads();
+    int es = is - cs, en = in - ne, tot_s = 0, tot_n = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+        if (w < warp) {
+            es += scan[w];
+            en += scan[8 + w];
+        }
+        tot_s += scan[w];
+        tot_n += scan[8 + w];
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int b = 4 * tid + j;
+        if (c[j] > 0) {
+            lst[en] = b;
+            off[en] = es;
+            cnt[b] = es;   // the bin's next free position
+            ++en;
+        }
+        es += c[j];
+    }
+    if (tid == 0) {
+        *g_out = tot_n;
+        off[tot_n] = tot_s;
+    }
+    __syncthreads();
+    // stable scatter of the slots, 32 at a time in ascending order, by one warp
+    if (warp == 0) {
+        for (int c0 = 0; c0 < S; c0 += 32) {
+            const int s = c0 + lane;
+            const int e = s < S ? a.ids[s] : -1;
+            const bool v = e >= 0 && e < N;
+            const uint32_t peers = __match_any_sync(kFull, v ? e : -2 - lane);
+            const int rank = __popc(peers & ((1u << lane) - 1u));
+            const int base = v ? cnt[e] : 0;
+            if (v) ord[base + rank] = s;
+            __syncwarp();
+            if (v && rank == 0) cnt[e] = base + __popc(peers);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+}
+
 // ==================================================================== the kernel
 
 template <bool F8>
@@ -321,10 +409,25 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         }
     }
 
+    // The routing every role reads: the call's, or, for the deduplicating form from ids, the
+    // grouping this CTA builds here (the same in every CTA).
+    ExpertArgs ar = a;
+    if (a.mode == kModeDedupIds) {
+        int32_t *const grp = reinterpret_cast<int32_t *>(base_ptr + kGrpOff);
+        int32_t *const lst = grp, *const off = grp + kMaxFusedSlots, *const ord = grp + 2 * kMaxFusedSlots + 1;
+        int32_t *const gcount = grp + 3 * kMaxFusedSlots + 1, *const scan = gcount + 1;
+        build_grouping(a, lst, off, ord, reinterpret_cast<int32_t *>(base_ptr + kCntOff), gcount, scan);
+        ar.mode = kModeDedup;
+        ar.expert_list = lst;
+        ar.offsets = off;
+        ar.slot_order = ord;
+        ar.num_distinct = gcount;
+    }
+
     using E = Elt<F8>;
     const int T = a.f / kFTile;
     const int KB = a.d / E::BK;
-    const int G = num_groups(a);
+    const int G = num_groups(ar);
     const int c = blockIdx.x;
     const int P = gridDim.x;
     // gate/up blocks: G*T items of KB k slices
@@ -365,7 +468,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         uint32_t cnt = 0;
         bool ok = true;
         for (long long b = glo; ok && b < ghi;) {
-            const Seg s = seg_at(a, b, ghi, KB, T);
+            const Seg s = seg_at(ar, b, ghi, KB, T);
             b = s.b1;
             if (!s.valid) continue;
             const int row = s.e * a.f + s.tile * kFTile;
@@ -388,7 +491,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             }
         }
         for (long long b = dlo; ok && b < dhi;) {
-            const Seg sg = seg_at(a, b, dhi, IB, T2);
+            const Seg sg = seg_at(ar, b, dhi, IB, T2);
             b = sg.b1;
             if (!sg.valid) continue;
             const Units u = units_of(sg);
@@ -418,7 +521,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         uint32_t cnt = 0, seg = 0;
         bool ok = true;
         for (long long b = glo; ok && b < ghi;) {
-            const Seg s = seg_at(a, b, ghi, KB, T);
+            const Seg s = seg_at(ar, b, ghi, KB, T);
             b = s.b1;
             if (!s.valid) continue;
             const uint32_t buf = seg & 1u, sph = (seg >> 1) & 1u;
@@ -452,7 +555,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         }
         uint32_t dcnt = 0, run = 0;
         for (long long b = dlo; ok && b < dhi;) {
-            const Seg sg = seg_at(a, b, dhi, IB, T2);
+            const Seg sg = seg_at(ar, b, dhi, IB, T2);
             b = sg.b1;
             if (!sg.valid) continue;
             const Units u = units_of(sg);
@@ -530,7 +633,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         // gate/up: y_part[row, t] of each item share, then its flag
         uint32_t seg = 0;
         for (long long b = glo; b < ghi;) {
-            const Seg s = seg_at(a, b, ghi, KB, T);
+            const Seg s = seg_at(ar, b, ghi, KB, T);
             b = s.b1;
             if (!s.valid) {
                 // reported once per group, by the CTA holding the group's first block
@@ -545,7 +648,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 rs = row < 64 ? a.s_gate[fr] : a.s_up[fr];
             }
             GroupInfo gi;
-            group_tokens(a, s.g, lane, gi);
+            group_tokens(ar, s.g, lane, gi);
             // this CTA's share of the item: 0 for the CTA holding its first block
             const int slot = c - gsp.part_of(static_cast<long long>(s.item) * KB);
             const uint32_t buf = seg & 1u, sph = (seg >> 1) & 1u;
@@ -583,7 +686,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         }
         uint32_t dcnt = 0, run = 0;
         for (long long b = dlo; ok && b < dhi;) {
-            const Seg sg = seg_at(a, b, dhi, IB, T2);
+            const Seg sg = seg_at(ar, b, dhi, IB, T2);
             b = sg.b1;
             if (!sg.valid) continue;
             const Units u = units_of(sg);
@@ -665,14 +768,14 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         const int hw = warp - 6;
         uint32_t run = 0;
         for (long long b = dlo; b < dhi;) {
-            const Seg sg = seg_at(a, b, dhi, IB, T2);
+            const Seg sg = seg_at(ar, b, dhi, IB, T2);
             b = sg.b1;
             if (!sg.valid) continue;
             const uint32_t rr = run++;
             if (static_cast<int>(rr & 1u) != hw) continue;
             const uint32_t hb = rr % kHRing, hph = (rr / kHRing) & 1u;
             GroupInfo gi;
-            group_tokens(a, sg.g, lane, gi);
+            group_tokens(ar, sg.g, lane, gi);
             const int nreal = min(kDnSub, T - sg.tile * kDnSub);
             // the CTA shares of each real tile's gate/up item: first CTA and count
             int p0[kDnSub], span[kDnSub];

@@ -1,0 +1,87 @@
+"""The deduplicating form from ids in one launch (moe_expert_op_dedup_ids and its e4m3 form):
+the grouping built inside the tensor-core kernel gives the result of moe_group_slots followed
+by moe_expert_op_dedup, including repeated and out-of-range ids, and the oracle's per token."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import TOL_BF16, DeviceLayer, rel_max_err, route
+from moe_speculative_decoding_gb300 import api, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from moe_speculative_decoding_gb300 import build
+    build.build()
+    api.lib()
+
+
+def test_repeated_and_bad_ids_match_the_two_calls(oracle_mod):
+    """A token naming one expert twice (its gates add), ids N and -1 (skipped, MOE_ERR_BAD_ID)."""
+    dl = DeviceLayer(256, 256, 16, 4, "bf16", seed=700)
+    n = 6
+    x = dl.activations(n, seed=701)
+    ids_np = np.array([[0, 1, 2, 3], [3, 3, 5, 7], [15, 14, 0, 1], [16, 2, -1, 9], [8, 8, 8, 8], [1, 4, 6, 12]],
+                      np.int32)
+    gates = torch.from_numpy(np.random.default_rng(2).random((n, 4)).astype(np.float32)).cuda()
+    ids = torch.from_numpy(ids_np).cuda()
+    grp = api.group_slots(ids, dl.N, ws=dl.ws)
+    y2 = api.expert_op_dedup(dl.layer, dl.w, x, gates, grp, ws=dl.ws).cpu().numpy()
+    assert api.last_device_error(dl.ws) == 5
+    y1 = api.expert_op_dedup_ids(dl.layer, dl.w, x, ids, gates, ws=dl.ws).cpu().numpy()
+    assert api.last_device_error(dl.ws) == 5
+    assert rel_max_err(y1, y2) <= 1e-4
+    ok = np.where((ids_np >= 0) & (ids_np < dl.N), ids_np, 0)
+    g = np.where((ids_np >= 0) & (ids_np < dl.N), gates.cpu().numpy(), 0.0)
+    ref = oracle_mod.expert_op_perslot(*dl.host(), synth.host_array(x), ok, g)
+    assert rel_max_err(y1, ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("n", [1, 3, 16])
+def test_qwen3_shape_matches_oracle_and_overwrite(oracle_mod, n):
+    """N = 128 experts, m = 8, d = 2048, f = 768 (smaller N for host copies: 32 experts)."""
+    dl = DeviceLayer(2048, 768, 32, 8, "bf16", seed=710 + n)
+    x = dl.activations(n, seed=711)
+    _, logits = synth.routing_traces(1, n, 32, 8, 0.4, seed=712 + n)
+    ids, gates = route(logits[0], 8)
+    y = torch.full((n, 2048), 7.0, device="cuda")
+    api.expert_op_dedup_ids(dl.layer, dl.w, x, ids, gates, y=y, ws=dl.ws)   # overwrite
+    y1 = y.cpu().numpy()
+    ref = oracle_mod.expert_op_perslot(*dl.host(), synth.host_array(x), ids.cpu().numpy(), gates.cpu().numpy())
+    assert rel_max_err(y1, ref) <= TOL_BF16
+    api.expert_op_dedup_ids(dl.layer, dl.w, x, ids, gates, y=y, accumulate=True, ws=dl.ws)
+    assert rel_max_err(y.cpu().numpy(), 2 * ref) <= TOL_BF16
+
+
+def test_e4m3_matches_the_two_calls():
+    d, f, N, m, n = 2048, 768, 32, 8, 16
+    dl = DeviceLayer(d, f, N, m, "bf16", seed=720)
+    l8 = api.make_layer(d, f, N, m, "e4m3")
+    ws8 = api.workspace(l8, 16, "cuda")
+    w8, sc = api.quantize_experts(dl.w)
+    x = dl.activations(n, seed=721)
+    xq, sx = api.quantize_rows_e4m3(x)
+    _, logits = synth.routing_traces(1, n, N, m, 0.4, seed=722)
+    ids, gates = route(logits[0], m)
+    grp = api.group_slots(ids, N)
+    y2 = api.expert_op_dedup_fp8(l8, w8, sc, xq, sx, gates, grp, ws=ws8).cpu().numpy()
+    y1 = api.expert_op_dedup_ids_fp8(l8, w8, sc, xq, sx, ids, gates, ws=ws8).cpu().numpy()
+    assert api.last_device_error(ws8) == 0
+    assert rel_max_err(y1, y2) <= 1e-4
+
+
+def test_unsupported_shapes():
+    f32 = api.make_layer(256, 512, 8, 2, "f32")
+    dl = DeviceLayer(256, 512, 8, 2, "f32", seed=730)
+    x = dl.activations(4, seed=731)
+    ids = torch.zeros((4, 2), dtype=torch.int32, device="cuda")
+    gates = torch.ones((4, 2), device="cuda")
+    with pytest.raises(api.MoeError):
+        api.expert_op_dedup_ids(f32, dl.w, x, ids, gates, ws=dl.ws)
+    big = DeviceLayer(256, 128, 64, 32, "bf16", seed=732)
+    xb = big.activations(9, seed=733)
+    with pytest.raises(api.MoeError):   # n m = 288 > 256
+        api.expert_op_dedup_ids(big.layer, big.w, xb, torch.zeros((9, 32), dtype=torch.int32, device="cuda"),
+                                torch.ones((9, 32), device="cuda"), ws=big.ws)

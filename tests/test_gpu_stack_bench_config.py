@@ -1,7 +1,8 @@
 """Parity at the bench's full size and in the launch configuration bench.py times: the
-48-layer Qwen3-30B-A3B-shaped stack (57.98 GB resident), CUDA-graph replays of the four
-phases (route over all layers' tokens, 48 per-slot launches, 48 groupings, 48 dedup
-launches), checked on sampled layers and tokens against the oracle one token at a time."""
+48-layer Qwen3-30B-A3B-shaped stack (57.98 GB resident), CUDA-graph replays of the timed
+phases (route over all layers' tokens, 48 per-slot launches, 48 deduplicating launches that
+group their slots themselves), checked on sampled layers and tokens against the oracle one
+token at a time; the standalone grouping of the same window checks U."""
 import os
 import sys
 
@@ -27,6 +28,8 @@ def stack():
                          device=torch.device("cuda", 0), use_graph=True)
     b.capture()
     b.step(1)               # the second window, as a timed step would
+    for n in b.n_values:    # the standalone grouping of the same window, for the U check
+        b._run(n, "group")
     torch.cuda.synchronize()
     assert api.last_device_error(b.ws) == 0
     yield b
