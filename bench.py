@@ -315,6 +315,31 @@ def fp8_leg(b: "StackBench", args, device, per_n_bf16):
                 launches_per_layer_form=2)
 
 
+def read_probe_leg(device, gib: int = 4, reps: int = 5):
+    """Read-only streaming probe (our TMA bulk-copy kernel) over a 4 GiB buffer: the read
+    bandwidth beside the copy peak (read + write) of MEASURED_PEAKS.json."""
+    buf = torch.empty(gib << 30, dtype=torch.uint8, device=device)
+    buf.fill_(1)
+    ws = api.workspace(api.make_layer(256, 256, 8, 2), 1, device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    api.read_probe(buf, ws)
+    ts = []
+    for _ in range(reps):
+        torch.cuda.synchronize(device)
+        ev[0].record()
+        nbytes = api.read_probe(buf, ws)
+        ev[1].record()
+        torch.cuda.synchronize(device)
+        ts.append(ev[0].elapsed_time(ev[1]) * 1e-3)
+    assert api.last_device_error(ws) == 0
+    t = float(np.median(ts))
+    del buf
+    torch.cuda.empty_cache()
+    return dict(gbs=round(nbytes / t / 1e9, 1), bytes=int(nbytes), us=round(t * 1e6, 1),
+                of_copy_peak=round(nbytes / t / 1e9 / measured_peaks()[0]["hbm_gbs"], 4),
+                kernel="read_probe_kernel (1-D TMA bulk copies, one CTA per SM)")
+
+
 def verify_side_leg(device, reps: int = 20, B: int = 16, K: int = 8, V: int = 151936, nodes: int = 18,
                     layers: int = 48, N: int = 128, m: int = 8):
     """The steps either side of the verification pass, timed on the device.
@@ -727,6 +752,8 @@ def run_ours(args, world, rank, local):
         line["fp8"] = fp8_leg(b, args, device, per_n)
     if rank == 0 and not args.no_fit:
         line["fits"] = fit_leg(wl, b.weights[0], device, reps=args.fit_reps)
+    if rank == 0:
+        line["hbm_read_probe"] = read_probe_leg(device)
     if rank == 0 and not args.no_verify_side:
         line["verify_side"] = verify_side_leg(device, reps=args.verify_reps)
     if rank == 0 and not args.no_cpu_baseline and world == 1:

@@ -11,9 +11,11 @@
  *  * Ownership: the caller owns every buffer (device or host).  The library never
  *    allocates or frees device memory; scratch comes from a caller-provided workspace
  *    of moe_workspace_bytes() bytes.
- *  * Pointers marked [dev] are device pointers, [host] host pointers.  Every device
- *    buffer must be 16-byte aligned; weight and activation buffers must also be
- *    contiguous row-major in the layouts stated below.
+ *  * Pointers marked [dev] are device pointers, [host] host pointers.  Weights, x, y and
+ *    workspaces must be 16-byte aligned; routing arrays (logits, ids, gates, the grouping)
+ *    and scale arrays, which the kernels read one element at a time, need only 4-byte
+ *    alignment (so per-layer slices of one ids array stay valid for any n and m).  Weight
+ *    and activation buffers must also be contiguous row-major in the layouts stated below.
  *  * Asynchrony: a call that takes a stream enqueues its kernels on that stream and
  *    returns without synchronising.  The host-only calls and moe_last_device_error (which
  *    synchronises the stream) are the exceptions.
@@ -232,8 +234,8 @@ typedef struct {
  * experts of [Lan, App. E Table 6], in GB300's FP8 tensor-core format): as
  * moe_expert_op_perslot / moe_expert_op_dedup, with
  *   w_gate, w_up, w_down [dev] e4m3 codes in the layouts of moe_layer_t, scales their row scales;
- *   x [dev] uint8 [n, d] e4m3 codes, x_scale [dev] fp32 [n] the token scales (scale arrays
- *   need only 4-byte alignment; every other pointer 16 bytes, as elsewhere).
+ *   x [dev] uint8 [n, d] e4m3 codes, x_scale [dev] fp32 [n] the token scales (alignment as
+ *   stated at the top: scale arrays 4 bytes).
  * h is rounded to e4m3 as the down projection's operand, with one scale per token and
  * 128-wide block of f (amax / 448).  layer->w_dtype = layer->x_dtype = MOE_E4M3, d and f
  * multiples of 128; requested bytes per expert w = 3 d f + 4 (2 f + d) (moe_pass_bytes).
@@ -416,6 +418,16 @@ moe_status_t moe_fit_op_times(int32_t count, const int32_t *n, const int32_t *U,
  * (a moe_status_t value; MOE_OK if nothing was recorded) and clears it.
  */
 moe_status_t moe_last_device_error(void *ws, moe_stream_t s, int32_t *code);
+
+/*
+ * Measurement helper, not part of the method: a read-only streaming probe.  One CTA per SM
+ * streams its contiguous share of buf through 1-D TMA bulk copies into shared memory and
+ * discards it: floor(bytes / 32768) * 32768 bytes are read.  Time it on the stream to get the
+ * read bandwidth the expert kernel's weight stream can reach, beside a copy's (read + write).
+ *   buf [dev] 16-byte aligned, bytes >= 32768; ws [dev] a workspace (its error word records a
+ *   wait that timed out).  Asynchronous on s.
+ */
+moe_status_t moe_read_probe(const void *buf, size_t bytes, void *ws, moe_stream_t s);
 
 /* ---------------------------------------------------------------- verify-side neighbours */
 

@@ -69,7 +69,7 @@ EXPORTED = ("moe_abi_version", "moe_status_str", "moe_workspace_bytes", "moe_wor
             "moe_error_bounds", "moe_kstar_separated", "moe_fit_op_times", "moe_expert_op_perslot_fp8",
             "moe_expert_op_dedup_fp8", "moe_quantize_rows_e4m3", "moe_spec_accept",
             "moe_union_cost_workspace_bytes", "moe_union_cost", "moe_expert_op_dedup_ids",
-            "moe_expert_op_dedup_ids_fp8")
+            "moe_expert_op_dedup_ids_fp8", "moe_read_probe")
 
 _lib = None
 
@@ -121,6 +121,7 @@ def lib():
         "moe_expert_op_dedup_ids_fp8": ([LP, P, P, P, ctypes.POINTER(WeightScales), P, P, P, P, I32, I32, P, P, SZ, P],
                                         I32),
         "moe_union_cost_workspace_bytes": ([I32], SZ),
+        "moe_read_probe": ([P, SZ, P, P], I32),
         "moe_union_cost": ([P, I32, I32, I32, P, I32, P, P, D, P, P, P, P, P, P, SZ, P], I32),
     }
     for name, (args, res) in sig.items():
@@ -498,3 +499,11 @@ def union_cost(bitmaps, subsets, pv, bcoef, beta: float, out=None, ws=None):
                                 _dev(out["best"], "best", torch.int32), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                                 _stream(dev)), "moe_union_cost")
     return out
+
+
+def read_probe(buf: torch.Tensor, ws: torch.Tensor) -> int:
+    """Enqueue the read-only streaming probe over buf (a CUDA tensor); returns the bytes it reads."""
+    nbytes = buf.numel() * buf.element_size()
+    _check(lib().moe_read_probe(ctypes.c_void_p(buf.data_ptr()), nbytes, ctypes.c_void_p(ws.data_ptr()),
+                                _stream(buf.device)), "moe_read_probe")
+    return nbytes // 32768 * 32768

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmoeverify.so")
-SOURCES = ("api.cu", "route.cu", "group.cu", "expert_simt.cu", "expert_tc.cu", "noalloc.cu", "quant.cu", "spec.cu")
+SOURCES = ("api.cu", "route.cu", "group.cu", "expert_simt.cu", "expert_tc.cu", "noalloc.cu", "quant.cu", "spec.cu", "probe.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -15,6 +15,10 @@
 #include "spec_args.cuh"
 
 namespace moe {
+cudaError_t launch_read_probe(const void *buf, size_t bytes, int32_t *err, cudaStream_t s);
+}
+
+namespace moe {
 cudaError_t launch_route_topm(const float *logits, int n, int N, int m, int renorm, int32_t *ids, float *gates,
                               cudaStream_t s, bool pdl);
 cudaError_t launch_group_slots(const int32_t *ids, int S, int N, int32_t *num_distinct, int32_t *expert_list,
@@ -30,6 +34,8 @@ namespace {
 constexpr bool kUsePdl = true;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// ids, gates, logits and groupings are read one element at a time: 4-byte alignment suffices
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
@@ -63,9 +69,10 @@ moe_status_t check_expert_common(const moe_layer_t *L, const void *wg, const voi
     if (st != MOE_OK) return st;
     if (n < 1) return MOE_ERR_ARG;
     if (n > MOE_MAX_PASS_TOKENS) return MOE_ERR_UNSUPPORTED;
-    const void *ptrs[] = {wg, wu, wd, x, gates, y};
+    const void *ptrs[] = {wg, wu, wd, x, y};
     for (const void *p : ptrs)
         if (p == nullptr || !aligned16(p)) return MOE_ERR_ARG;
+    if (gates == nullptr || !aligned4(gates)) return MOE_ERR_ARG;
     if (ws == nullptr || ws_bytes < moe_workspace_bytes(L, n)) return MOE_ERR_WORKSPACE;
     if (!aligned16(ws)) return MOE_ERR_ARG;
     return MOE_OK;
@@ -152,7 +159,7 @@ moe_status_t moe_route_topm(const float *logits, int32_t n, int32_t N, int32_t m
     if (m > N || N > 1024 || m > 32) return MOE_ERR_UNSUPPORTED;
     if (n == 0) return MOE_OK;
     if (logits == nullptr || ids == nullptr || gates == nullptr) return MOE_ERR_ARG;
-    if (!aligned16(logits) || !aligned16(ids) || !aligned16(gates)) return MOE_ERR_ARG;
+    if (!aligned4(logits) || !aligned4(ids) || !aligned4(gates)) return MOE_ERR_ARG;
     cudaError_t e = launch_route_topm(logits, n, N, m, renorm, ids, gates, reinterpret_cast<cudaStream_t>(s), kUsePdl);
     if (e == cudaSuccess) e = cudaGetLastError();
     return cuda_status(e);
@@ -165,7 +172,7 @@ moe_status_t moe_group_slots(const int32_t *ids, int32_t n, int32_t m, int32_t N
     if (static_cast<int64_t>(n) * m > 4096 || N > 1024) return MOE_ERR_UNSUPPORTED;
     const void *ptrs[] = {ids, num_distinct, expert_list, expert_offsets, slot_order};
     for (const void *p : ptrs)
-        if (p == nullptr || !aligned16(p)) return MOE_ERR_ARG;
+        if (p == nullptr || !aligned4(p)) return MOE_ERR_ARG;
     if (ws != nullptr && !aligned16(ws)) return MOE_ERR_ARG;
     int32_t *err = ws ? &static_cast<DeviceWorkspace *>(ws)->error : nullptr;
     cudaError_t e = launch_group_slots(ids, n * m, N, num_distinct, expert_list, expert_offsets, slot_order, err,
@@ -181,7 +188,7 @@ moe_status_t moe_expert_op_perslot(const moe_layer_t *layer, const void *w_gate,
     moe_status_t st = check_expert_common(layer, w_gate, w_up, w_down, x, gates, n, y, ws, ws_bytes);
     if (st != MOE_OK) return st;
     if (is_fp8(layer)) return MOE_ERR_UNSUPPORTED;   // e4m3 needs its scales: the _fp8 call
-    if (ids == nullptr || !aligned16(ids)) return MOE_ERR_ARG;
+    if (ids == nullptr || !aligned4(ids)) return MOE_ERR_ARG;
     ExpertArgs a = make_args(layer, w_gate, w_up, w_down, x, gates, n, y, ws, kModePerSlot);
     a.ids = ids;
     return run_expert(layer, a, n * layer->m, accumulate, ws, reinterpret_cast<cudaStream_t>(s));
@@ -197,7 +204,7 @@ moe_status_t moe_expert_op_dedup(const moe_layer_t *layer, const void *w_gate, c
     if (is_fp8(layer)) return MOE_ERR_UNSUPPORTED;   // e4m3 needs its scales: the _fp8 call
     const void *ptrs[] = {num_distinct, expert_list, expert_offsets, slot_order};
     for (const void *p : ptrs)
-        if (p == nullptr || !aligned16(p)) return MOE_ERR_ARG;
+        if (p == nullptr || !aligned4(p)) return MOE_ERR_ARG;
     ExpertArgs a = make_args(layer, w_gate, w_up, w_down, x, gates, n, y, ws, kModeDedup);
     a.num_distinct = num_distinct;
     a.expert_list = expert_list;
@@ -214,7 +221,7 @@ moe_status_t moe_expert_op_dedup_ids(const moe_layer_t *layer, const void *w_gat
     moe_status_t st = check_expert_common(layer, w_gate, w_up, w_down, x, gates, n, y, ws, ws_bytes);
     if (st != MOE_OK) return st;
     if (is_fp8(layer) || !uses_tc(layer) || n * layer->m > kMaxFusedSlots) return MOE_ERR_UNSUPPORTED;
-    if (ids == nullptr || !aligned16(ids)) return MOE_ERR_ARG;
+    if (ids == nullptr || !aligned4(ids)) return MOE_ERR_ARG;
     ExpertArgs a = make_args(layer, w_gate, w_up, w_down, x, gates, n, y, ws, kModeDedupIds);
     a.ids = ids;
     const int cap = n * layer->m < layer->N ? n * layer->m : layer->N;
@@ -223,8 +230,6 @@ moe_status_t moe_expert_op_dedup_ids(const moe_layer_t *layer, const void *w_gat
 
 namespace {
 // the kernels read scales one fp32 at a time: 4-byte alignment suffices
-bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
-
 bool fp8_scales_ok(const moe_weight_scales_t *sc, const float *x_scale) {
     return sc != nullptr && sc->gate != nullptr && sc->up != nullptr && sc->down != nullptr && x_scale != nullptr &&
            aligned4(sc->gate) && aligned4(sc->up) && aligned4(sc->down) && aligned4(x_scale);
@@ -238,7 +243,7 @@ moe_status_t moe_expert_op_perslot_fp8(const moe_layer_t *layer, const void *w_g
     moe_status_t st = check_expert_common(layer, w_gate, w_up, w_down, x, gates, n, y, ws, ws_bytes);
     if (st != MOE_OK) return st;
     if (!is_fp8(layer)) return MOE_ERR_UNSUPPORTED;
-    if (ids == nullptr || !aligned16(ids) || !fp8_scales_ok(scales, x_scale)) return MOE_ERR_ARG;
+    if (ids == nullptr || !aligned4(ids) || !fp8_scales_ok(scales, x_scale)) return MOE_ERR_ARG;
     ExpertArgs a = make_args(layer, w_gate, w_up, w_down, x, gates, n, y, ws, kModePerSlot);
     a.ids = ids;
     a.s_gate = scales->gate;
@@ -255,7 +260,7 @@ moe_status_t moe_expert_op_dedup_ids_fp8(const moe_layer_t *layer, const void *w
     moe_status_t st = check_expert_common(layer, w_gate, w_up, w_down, x, gates, n, y, ws, ws_bytes);
     if (st != MOE_OK) return st;
     if (!is_fp8(layer) || n * layer->m > kMaxFusedSlots) return MOE_ERR_UNSUPPORTED;
-    if (ids == nullptr || !aligned16(ids) || !fp8_scales_ok(scales, x_scale)) return MOE_ERR_ARG;
+    if (ids == nullptr || !aligned4(ids) || !fp8_scales_ok(scales, x_scale)) return MOE_ERR_ARG;
     ExpertArgs a = make_args(layer, w_gate, w_up, w_down, x, gates, n, y, ws, kModeDedupIds);
     a.ids = ids;
     a.s_gate = scales->gate;
@@ -277,7 +282,7 @@ moe_status_t moe_expert_op_dedup_fp8(const moe_layer_t *layer, const void *w_gat
     if (!is_fp8(layer)) return MOE_ERR_UNSUPPORTED;
     const void *ptrs[] = {num_distinct, expert_list, expert_offsets, slot_order};
     for (const void *p : ptrs)
-        if (p == nullptr || !aligned16(p)) return MOE_ERR_ARG;
+        if (p == nullptr || !aligned4(p)) return MOE_ERR_ARG;
     if (!fp8_scales_ok(scales, x_scale)) return MOE_ERR_ARG;
     ExpertArgs a = make_args(layer, w_gate, w_up, w_down, x, gates, n, y, ws, kModeDedup);
     a.num_distinct = num_distinct;
@@ -631,6 +636,14 @@ moe_status_t moe_union_cost(const uint64_t *bitmaps, int32_t nodes, int32_t L, i
     a.count = count;
     cudaError_t e = launch_union_cost(a, ws, st, kUsePdl);
     if (e == cudaSuccess) e = cudaGetLastError();
+    return cuda_status(e);
+}
+
+moe_status_t moe_read_probe(const void *buf, size_t bytes, void *ws, moe_stream_t s) {
+    if (buf == nullptr || !aligned16(buf) || ws == nullptr || !aligned16(ws)) return MOE_ERR_ARG;
+    if (bytes < 32768) return MOE_ERR_ARG;
+    cudaError_t e = launch_read_probe(buf, bytes, &static_cast<DeviceWorkspace *>(ws)->error,
+                                      reinterpret_cast<cudaStream_t>(s));
     return cuda_status(e);
 }
 

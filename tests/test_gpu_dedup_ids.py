@@ -85,3 +85,23 @@ def test_unsupported_shapes():
     with pytest.raises(api.MoeError):   # n m = 288 > 256
         api.expert_op_dedup_ids(big.layer, big.w, xb, torch.zeros((9, 32), dtype=torch.int32, device="cuda"),
                                 torch.ones((9, 32), device="cuda"), ws=big.ws)
+
+
+def test_routing_slices_need_only_element_alignment(oracle_mod):
+    """Per-layer slices of one ids / gates array start 8 bytes apart when m = 2 and n is odd:
+    every form takes them (the kernels read routing arrays one element at a time)."""
+    dl = DeviceLayer(512, 256, 8, 2, "bf16", seed=740)
+    n = 3
+    x = dl.activations(n, seed=741)
+    _, logits = synth.routing_traces(1, 2 * n, 8, 2, 0.3, seed=742)
+    ids_all, gates_all = route(logits[0], 2)
+    ids, gates = ids_all[n:], gates_all[n:]             # 24-byte offset: 8-byte aligned only
+    assert ids.data_ptr() % 16 == 8
+    ref = oracle_mod.expert_op_perslot(*dl.host(), synth.host_array(x), ids.cpu().numpy(), gates.cpu().numpy())
+    ys = api.expert_op_perslot(dl.layer, dl.w, x, ids, gates, ws=dl.ws).cpu().numpy()
+    grp = api.group_slots(ids, 8, ws=dl.ws)
+    yd = api.expert_op_dedup(dl.layer, dl.w, x, gates, grp, ws=dl.ws).cpu().numpy()
+    yi = api.expert_op_dedup_ids(dl.layer, dl.w, x, ids, gates, ws=dl.ws).cpu().numpy()
+    assert api.last_device_error(dl.ws) == 0
+    for y in (ys, yd, yi):
+        assert rel_max_err(y, ref) <= TOL_BF16

@@ -73,3 +73,23 @@ def test_no_alloc_reports_device_errors_per_call(noalloc):
     assert int(status.item()) == 0          # cleared at the start of the next call
     y_ws = api.expert_op_perslot(dl.layer, dl.w, x, good, gates, ws=dl.ws).cpu().numpy()
     assert rel_max_err(y.cpu().numpy(), y_ws) <= 1e-4
+
+
+def test_no_alloc_alternating_layer_shapes(noalloc):
+    """Calls that alternate between layers of different (f, m) share the scratch: its
+    tensor-core flag region moves with the shape and starts from zero after every change, so
+    every call still matches the workspace call."""
+    a = DeviceLayer(1024, 768, 32, 8, "bf16", seed=520)
+    b = DeviceLayer(1024, 256, 16, 2, "bf16", seed=521)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for rep in range(3):
+        for dl, n in ((a, 16), (b, 5), (a, 3), (b, 16)):
+            x = dl.activations(n, seed=522 + rep + n)
+            _, logits = synth.routing_traces(1, n, dl.N, dl.m, 0.4, seed=523 + rep + n)
+            ids, gates = route(logits[0], dl.m)
+            y_ref = api.expert_op_perslot(dl.layer, dl.w, x, ids, gates, ws=dl.ws).cpu().numpy()
+            y = torch.full((n, dl.d), float("nan"), dtype=torch.float32, device="cuda")
+            assert _call(noalloc, dl.layer, dl.w, x, ids, gates, y, status) == 0
+            torch.cuda.synchronize()
+            assert int(status.item()) == 0
+            assert rel_max_err(y.cpu().numpy(), y_ref) <= 1e-4
