@@ -237,7 +237,7 @@ typedef struct {
  *   x [dev] uint8 [n, d] e4m3 codes, x_scale [dev] fp32 [n] the token scales (alignment as
  *   stated at the top: scale arrays 4 bytes).
  * h is rounded to e4m3 as the down projection's operand, with one scale per token and
- * 128-wide block of f (amax / 448).  layer->w_dtype = layer->x_dtype = MOE_E4M3, d and f
+ * 256-wide block of f (amax / 448; the last block is 128 wide when f % 256 = 128).  layer->w_dtype = layer->x_dtype = MOE_E4M3, d and f
  * multiples of 128; requested bytes per expert w = 3 d f + 4 (2 f + d) (moe_pass_bytes).
  * Returns MOE_ERR_UNSUPPORTED for a layer that is not e4m3.
  */

@@ -35,10 +35,11 @@
 //
 // FP8 layers (e4m3 weights and x, one fp32 scale per weight row and per token) use the same
 // kernel instantiated for kind::f8f6f4: a 128-byte row then holds 128 elements, so a
-// gate/up block is a 128-wide k slice and one down block covers the item's whole 128-wide
-// f span.  The gate/up epilogue applies the row and token scales to its partial sums; the
-// h formers quantize h per (token, 128-wide f span) with scale amax/448, and the down
-// epilogue applies that scale and the W_down row scale.
+// gate/up block is a 128-wide k slice, a down block a 128-wide f slice, and a down item
+// (two blocks per unit) spans 256 f.  The gate/up epilogue applies the row and token scales
+// to its partial sums; the h formers quantize h per (token, item) with scale amax/448 (one
+// scale for both blocks a unit accumulates), and the down epilogue applies that scale and
+// the W_down row scale.
 //
 // The flags need no clearing between calls: every call takes a new ticket (the workspace's
 // epoch word plus one), and the last CTA to start stores it back as the epoch.  All CTAs
@@ -65,22 +66,23 @@ constexpr int kStages = 11;                   // ring slots
 constexpr int kDownBufs = 8;                  // TMEM ring of down-block accumulators
 constexpr int kEpiBatch = 4;                  // down blocks per epilogue round
 constexpr int kHRing = 4;
-constexpr int kDnSub = 2;                     // f tiles per down item: blocks of one d block accumulate
+constexpr int kUnit = 2;                      // down blocks per TMEM accumulator (a unit)
 constexpr uint32_t kHBytes = kNT * 128;       // one h tile: 16 rows x 128 B
-constexpr uint32_t kHEntry = kDnSub * kHBytes;
+constexpr uint32_t kHEntry = kUnit * kHBytes;
 constexpr uint32_t kInfoBytes = 144;          // mask, the 16 gates, the 16 h scales (FP8)
-constexpr uint32_t kTmemCols = 256;           // gate/up accumulators at columns 0-31, down at 32-159
-constexpr uint32_t kDnCol0 = 32;
+constexpr int kGuBufs = 4;                    // TMEM ring of gate/up item accumulators
+constexpr uint32_t kTmemCols = 256;           // gate/up accumulators at columns 0-63, down at 64-191
+constexpr uint32_t kDnCol0 = 16 * kGuBufs;
 constexpr long long kDrainCycles = 400000000ll;   // about 0.2 s
 
 // Shared memory: the ring, kHRing h entries, their group records, each epilogue warp's copy
-// of the token scales (FP8), then barriers full[S], empty[S], gacc_full[2], gacc_empty[2],
+// of the token scales (FP8), then barriers full[S], empty[S], gacc_full[G], gacc_empty[G],
 // dacc_full[B], dacc_empty[B], h_full[R], h_empty[R], drain, then the misc words.
 constexpr uint32_t kHOff = kStages * kSlotBytes;
 constexpr uint32_t kInfoOff = kHOff + kHRing * kHEntry;
 constexpr uint32_t kSxOff = kInfoOff + kHRing * kInfoBytes;
 constexpr uint32_t kBarOff = kSxOff + 4 * kNT * 4;
-constexpr int kNumBars = 2 * kStages + 4 + 2 * kDownBufs + 2 * kHRing + 1;
+constexpr int kNumBars = 2 * kStages + 2 * kGuBufs + 2 * kDownBufs + 2 * kHRing + 1;
 constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
 // the grouping of the deduplicating form from ids: expert list, offsets, slot order, the count,
 // two scan scratch rows, then the per-expert counts (N <= 1024)
@@ -98,8 +100,13 @@ template <bool F8>
 struct Elt {
     static constexpr int BK = F8 ? 128 : 64;   // k elements per 128-byte row of an operand tile
     static constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(128, kNT) : idesc_bf16_f32(128, kNT);
-    // down blocks per unit: two 64-wide f tiles of bf16, or one 128-wide tile of e4m3
-    static constexpr int UNIT = F8 ? 1 : 2;
+    // a down block spans TPB 64-row gate/up tiles of f (one 128-byte row of W_down: 64 bf16 or
+    // 128 e4m3), a unit kUnit blocks, a down item ITEM tiles: 128 f (bf16) or 256 f (e4m3)
+    static constexpr int TPB = F8 ? 2 : 1;
+    static constexpr int UNIT = kUnit;
+    static constexpr int ITEM = kUnit * TPB;
+    static constexpr int COLS = ITEM * 64 / 32;   // f columns of an item per h-former lane
+    static constexpr int TK = F8 ? 2 : 4;         // tokens per round of the h formers' loads
     __device__ __forceinline__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
         if constexpr (F8) tc_mma_f8(d, a, b, IDESC, acc);
         else tc_mma_bf16(d, a, b, IDESC, acc);
@@ -341,9 +348,9 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     uint8_t *const info_ptr = base_ptr + kInfoOff;
     const uint32_t bar_full = base + kBarOff;
     const uint32_t bar_empty = bar_full + 8u * kStages;
-    const uint32_t bar_gacc_full = bar_empty + 8u * kStages;       // [2]
-    const uint32_t bar_gacc_empty = bar_gacc_full + 16u;           // [2]
-    const uint32_t bar_dacc_full = bar_gacc_empty + 16u;           // [kDownBufs]
+    const uint32_t bar_gacc_full = bar_empty + 8u * kStages;       // [kGuBufs]
+    const uint32_t bar_gacc_empty = bar_gacc_full + 8u * kGuBufs;  // [kGuBufs]
+    const uint32_t bar_dacc_full = bar_gacc_empty + 8u * kGuBufs;  // [kDownBufs]
     const uint32_t bar_dacc_empty = bar_dacc_full + 8u * kDownBufs;  // [kDownBufs]
     const uint32_t bar_h_full = bar_dacc_empty + 8u * kDownBufs;   // [kHRing]
     const uint32_t bar_h_empty = bar_h_full + 8u * kHRing;         // [kHRing]
@@ -360,7 +367,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             mbar_init(bar_full + 8u * s, 1);
             mbar_init(bar_empty + 8u * s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kGuBufs; ++b) {
             mbar_init(bar_gacc_full + 8u * b, 1);
             mbar_init(bar_gacc_empty + 8u * b, 4);      // the 4 epilogue warps
         }
@@ -435,9 +442,9 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     const long long glo = c < gsp.parts ? gsp.lo(c) : 0, ghi = c < gsp.parts ? gsp.lo(c + 1) : 0;
     // down blocks: G*T2 items of IB blocks, (d block ob, sub-tile s) with s innermost, so the
     // sub-tiles of one d block accumulate in one TMEM accumulator: a unit.  The last item of
-    // a group has fewer real sub-tiles when T is not a multiple of kDnSub; the others are
+    // a group has fewer real blocks when T is not a multiple of E::ITEM; the others are
     // skipped by every role alike.
-    const int T2 = (T + kDnSub - 1) / kDnSub;
+    const int T2 = (T + E::ITEM - 1) / E::ITEM;
     const int OBS = a.d / kOB;
     const int IB = OBS * E::UNIT;
     const long long nblk = static_cast<long long>(G) * T2 * IB;
@@ -456,9 +463,9 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         const long long ib0 = static_cast<long long>(sg.item) * IB;
         u.r0 = static_cast<int>(sg.b0 - ib0);
         u.r1 = static_cast<int>(sg.b1 - ib0);
-        // bf16: the item's 64-wide tiles present (the last item of a group may have one);
-        // e4m3: one block spans the item's 128 columns (f is a multiple of 128)
-        u.nreal = F8 ? 1 : min(kDnSub, T - sg.tile * kDnSub);
+        // the item's real blocks: the last item of a group may have one (f not a multiple of
+        // 128 for bf16, of 256 for e4m3)
+        u.nreal = min(E::ITEM, T - sg.tile * E::ITEM) / E::TPB;
         return u;
     };
 
@@ -505,7 +512,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                     if (elect_one()) {
                         const uint32_t fb = bar_full + 8u * st;
                         mbar_arrive_expect_tx(fb, kWBytes);
-                        tma_load_2d(base + st * kSlotBytes, &tm_wd, fb, (sg.tile * kDnSub + sub) * kFTile,
+                        tma_load_2d(base + st * kSlotBytes, &tm_wd, fb, (sg.tile * E::ITEM + sub * E::TPB) * kFTile,
                                     sg.e * a.d + ob * kOB);
                     }
                     __syncwarp();
@@ -524,7 +531,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             const Seg s = seg_at(ar, b, ghi, KB, T);
             b = s.b1;
             if (!s.valid) continue;
-            const uint32_t buf = seg & 1u, sph = (seg >> 1) & 1u;
+            const uint32_t buf = seg % kGuBufs, sph = (seg / kGuBufs) & 1u;
             ++seg;
             if (!warp_wait(bar_gacc_empty + 8u * buf, sph ^ 1u, abort_flag, a.err)) {
                 ok = false;
@@ -651,7 +658,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             group_tokens(ar, s.g, lane, gi);
             // this CTA's share of the item: 0 for the CTA holding its first block
             const int slot = c - gsp.part_of(static_cast<long long>(s.item) * KB);
-            const uint32_t buf = seg & 1u, sph = (seg >> 1) & 1u;
+            const uint32_t buf = seg % kGuBufs, sph = (seg / kGuBufs) & 1u;
             ++seg;
             // wait outcomes are made warp-uniform so the .sync.aligned TMEM loads stay converged
             if (!warp_wait(bar_gacc_full + 8u * buf, sph, abort_flag, a.err)) {
@@ -776,89 +783,100 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             const uint32_t hb = rr % kHRing, hph = (rr / kHRing) & 1u;
             GroupInfo gi;
             group_tokens(ar, sg.g, lane, gi);
-            const int nreal = min(kDnSub, T - sg.tile * kDnSub);
+            const int ntiles = min(E::ITEM, T - sg.tile * E::ITEM);   // real gate/up tiles of the item
+            const int tile0 = sg.tile * E::ITEM;
             // the CTA shares of each real tile's gate/up item: first CTA and count
-            int p0[kDnSub], span[kDnSub];
+            int p0[E::ITEM], span[E::ITEM];
 #pragma unroll
-            for (int sub = 0; sub < kDnSub; ++sub) {
-                const long long first = static_cast<long long>(sg.g * T + min(sg.tile * kDnSub + sub, T - 1)) * KB;
-                p0[sub] = gsp.part_of(first);
-                span[sub] = min(gsp.part_of(first + KB - 1) - p0[sub] + 1, kMaxSpan);
+            for (int tl = 0; tl < E::ITEM; ++tl) {
+                const long long first = static_cast<long long>(sg.g * T + min(tile0 + tl, T - 1)) * KB;
+                p0[tl] = gsp.part_of(first);
+                span[tl] = min(gsp.part_of(first + KB - 1) - p0[tl] + 1, kMaxSpan);
             }
-            // lane l waits for flag (tile l / 12, share (l % 12) / 4, warp l % 4)
-            const int fsub = lane / 12, fsl = (lane % 12) / 4;
-            const uint32_t *fp = nullptr;
-#pragma unroll
-            for (int sub = 0; sub < kDnSub; ++sub)
-                if (fsub == sub && sub < nreal && fsl < span[sub])
-                    fp = gu_flag(a.flags, sg.g * T + sg.tile * kDnSub + sub, fsl, lane & 3);
             if (!warp_wait(bar_h_empty + 8u * hb, hph ^ 1u, abort_flag, a.err)) break;
-            if (!warp_wait_ticket(fp, ticket, abort_flag, a.err)) break;
+            // the flags of the tiles' shares, 12 per tile (3 shares x 4 epilogue warps): flag
+            // l + 32 r waits in lane l, round r
+            bool flags_ok = true;
+#pragma unroll
+            for (int r = 0; r < (E::ITEM * 12 + 31) / 32; ++r) {
+                const int fi = lane + 32 * r, ftl = fi / 12, fsl = (fi % 12) / 4;
+                const uint32_t *fp = nullptr;
+#pragma unroll
+                for (int tl = 0; tl < E::ITEM; ++tl)
+                    if (ftl == tl && tl < ntiles && fsl < span[tl]) fp = gu_flag(a.flags, sg.g * T + tile0 + tl, fsl, fi & 3);
+                flags_ok = flags_ok && warp_wait_ticket(fp, ticket, abort_flag, a.err);
+            }
+            if (!flags_ok) break;
             uint8_t *const hp = h_ptr + hb * kHEntry;
             float hsc[kNT];             // e4m3: the run's h scale per token
 #pragma unroll
             for (int t = 0; t < kNT; ++t) hsc[t] = 1.0f;
             const int ntok = __popc(gi.mask);
-            // four of the group's tokens at a time: all loads first (predicated, independent)
+            // E::TK of the group's tokens at a time: all loads first (predicated, independent).
+            // Lane column k is c = lane + 32 k of the item: gate/up tile c / 64, row c % 64.
 #pragma unroll
-            for (int k0 = 0; k0 < kNT; k0 += 4) {
+            for (int k0 = 0; k0 < kNT; k0 += E::TK) {
                 if (k0 >= ntok) break;
-                uint32_t tk[4];
-                int pk[4];
+                uint32_t tk[E::TK];
+                int pk[E::TK];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < E::TK; ++j) {
                     tk[j] = nth_token(gi.mask, k0 + j);
                     pk[j] = 0;
 #pragma unroll
                     for (int t = 0; t < kNT; ++t) pk[j] = (tk[j] == static_cast<uint32_t>(t)) ? gi.pos[t] : pk[j];
                 }
-                float pg[4][4][kMaxSpan], pu[4][4][kMaxSpan];
+                float pg[E::TK][E::COLS][kMaxSpan], pu[E::TK][E::COLS][kMaxSpan];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < E::TK; ++j) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int sub = k >> 1, i = lane + 32 * (k & 1);
-                        const bool on = tk[j] < static_cast<uint32_t>(kNT) && sub < nreal;
-                        const float *const pp = part + part_index(pk[j], T, sg.tile * kDnSub + (on ? sub : 0), 0, i);
+                    for (int k = 0; k < E::COLS; ++k) {
+                        const int c = lane + 32 * k, tl = c >> 6, i = c & 63;
+                        const bool on = tk[j] < static_cast<uint32_t>(kNT) && tl < ntiles;
+                        const float *const pp = part + part_index(pk[j], T, tile0 + (on ? tl : 0), 0, i);
 #pragma unroll
                         for (int sl = 0; sl < kMaxSpan; ++sl) {
-                            const bool ld = on && sl < span[sub];
+                            const bool ld = on && sl < span[tl];
                             pg[j][k][sl] = ld ? __ldcg(pp + sl * 128) : 0.0f;
                             pu[j][k][sl] = ld ? __ldcg(pp + sl * 128 + 64) : 0.0f;
                         }
                     }
                 }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < E::TK; ++j) {
                     const uint32_t t = tk[j];
                     if (t >= static_cast<uint32_t>(kNT)) break;
-                    float hv[4];
+                    float hv[E::COLS];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
+                    for (int k = 0; k < E::COLS; ++k)
                         hv[k] = silu(pg[j][k][0] + pg[j][k][1] + pg[j][k][2]) * (pu[j][k][0] + pu[j][k][1] + pu[j][k][2]);
                     if constexpr (!F8) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int sub = k >> 1, i = lane + 32 * (k & 1);
-                            if (sub >= nreal) continue;
+                        for (int k = 0; k < E::COLS; ++k) {
+                            const int c = lane + 32 * k, blk = c >> 6, i = c & 63;
+                            if (blk >= ntiles) continue;
                             // 128-byte swizzle: row t of 128 bytes, 16-byte chunk (i/8) ^ (t%8)
-                            const uint32_t off = static_cast<uint32_t>(sub * kHBytes + (t >> 3) * 1024 + (t & 7) * 128 +
+                            const uint32_t off = static_cast<uint32_t>(blk * kHBytes + (t >> 3) * 1024 + (t & 7) * 128 +
                                                                        (((i >> 3) ^ (t & 7)) << 4) + (i & 7) * 2);
                             *reinterpret_cast<__nv_bfloat16 *>(hp + off) = __float2bfloat16_rn(hv[k]);
                         }
                     } else {
-                        // e4m3 h: the token's 128 values of the span share one scale, amax / 448,
-                        // reduced over the warp before any value is rounded
-                        float mx = fmaxf(fmaxf(fabsf(hv[0]), fabsf(hv[1])), fmaxf(fabsf(hv[2]), fabsf(hv[3])));
+                        // e4m3 h: the token's values over the item's 256 (or 128) columns share
+                        // one scale, amax / 448, reduced over the warp before any is rounded
+                        float mx = 0.0f;
+#pragma unroll
+                        for (int k = 0; k < E::COLS; ++k)
+                            if (((lane + 32 * k) >> 6) < ntiles) mx = fmaxf(mx, fabsf(hv[k]));
 #pragma unroll
                         for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
                         const float hs = mx > 0.0f ? mx / 448.0f : 1.0f;
 #pragma unroll
                         for (int tt = 0; tt < kNT; ++tt) hsc[tt] = (t == static_cast<uint32_t>(tt)) ? hs : hsc[tt];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int fl = lane + 32 * k;   // column inside the 128-wide span
-                            const uint32_t off = static_cast<uint32_t>((t >> 3) * 1024 + (t & 7) * 128 +
+                        for (int k = 0; k < E::COLS; ++k) {
+                            const int c = lane + 32 * k, blk = c >> 7, fl = c & 127;   // block of 128, column in it
+                            if ((c >> 6) >= ntiles) continue;
+                            const uint32_t off = static_cast<uint32_t>(blk * kHBytes + (t >> 3) * 1024 + (t & 7) * 128 +
                                                                        (((fl >> 4) ^ (t & 7)) << 4) + (fl & 15));
                             hp[off] = f32_to_e4m3(hv[k] / hs);
                         }
@@ -945,7 +963,7 @@ template <bool F8>
 cudaError_t launch(const ExpertArgs &a, int sms, int max_groups, bool zero_y, float *part, cudaStream_t s, bool pdl) {
     using E = Elt<F8>;
     const long long T = a.f / kFTile, OBS = a.d / kOB;
-    const long long T2 = (T + kDnSub - 1) / kDnSub;
+    const long long T2 = (T + E::ITEM - 1) / E::ITEM;
     // CTAs with work: up to 2*G*T gate/up shares, and at most one per down block
     const long long work = std::max<long long>(2ll * max_groups * T, static_cast<long long>(max_groups) * T2 * OBS * E::UNIT);
     const int grid = static_cast<int>(std::min<long long>(std::min(sms, kMaxGrid), work));
@@ -981,7 +999,7 @@ cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, f
     const bool bf = a.w_dtype == MOE_BF16 && a.x_dtype == MOE_BF16;
     if (!expert_tc_supports(a.d, a.f) || !(f8 || bf) || a.n > kNT || max_groups < 1) return cudaErrorNotSupported;
     if (a.sync == nullptr || a.flags == nullptr) return cudaErrorInvalidValue;
-    // e4m3: 128-element k slices and 128-wide f spans
+    // e4m3: 128-element k slices; h spans of 256 f (the last may be 128)
     if (f8 && (a.d % 128 != 0 || a.f % 128 != 0 || a.s_gate == nullptr || a.s_up == nullptr ||
                a.s_down == nullptr || a.s_x == nullptr))
         return cudaErrorNotSupported;

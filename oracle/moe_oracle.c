@@ -741,12 +741,15 @@ int oracle_expert_op_token_fp8(int d, int f, int N, int m, const uint8_t *wg, co
             u *= (double)su[(size_t)e * f + i] * (double)sx[t];
             h[i] = g / (1.0 + exp(-g)) * u;
         }
-        for (int b0 = 0; b0 < f; b0 += 128) {
+        /* h rounded to e4m3 per span of 256 columns of f (the last one 128 when f is not a
+         * multiple of 256), one scale amax / 448 per token and span */
+        for (int b0 = 0; b0 < f; b0 += 256) {
+            const int b1 = b0 + 256 < f ? b0 + 256 : f;
             float amax = 0.0f;
-            for (int i = b0; i < b0 + 128; ++i)
+            for (int i = b0; i < b1; ++i)
                 if (fabsf((float)h[i]) > amax) amax = fabsf((float)h[i]);
             float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
-            for (int i = b0; i < b0 + 128; ++i)
+            for (int i = b0; i < b1; ++i)
                 hq[i] = oracle_e4m3_decode(oracle_e4m3_encode((double)((float)h[i] / sc))) * (double)sc;
         }
         for (int o = 0; o < d; ++o) {

@@ -53,8 +53,13 @@ def test_fp8_expert_op_within_the_h_rounding_bound(oracle_mod):
     """y from the oracle equals the fp64 SwiGLU of the dequantized weights and x, with h
     replaced by its e4m3 rounding: |y - y_exact| <= sum_j |gate_j| |s_d[o]| sum_i |W_d[o][i]|
     (|h_i| 2^-4 + s_b 2^-10), a bound a dropped term or a swapped index would break."""
-    rng = np.random.default_rng(122)
-    E, d, f, n, m = 3, 64, 256, 3, 2
+    for f in (256, 384):   # one 256-wide span of h; a 256 and a trailing 128
+        _check_fp8_expert_bound(oracle_mod, f)
+
+
+def _check_fp8_expert_bound(oracle_mod, f):
+    rng = np.random.default_rng(122 + f)
+    E, d, n, m = 3, 64, 3, 2
     wg = (rng.normal(0, 1 / np.sqrt(d), (E * f, d))).astype(np.float32)
     wu = (rng.normal(0, 1 / np.sqrt(d), (E * f, d))).astype(np.float32)
     wd = (rng.normal(0, 1 / np.sqrt(f), (E * d, f))).astype(np.float32)
@@ -77,7 +82,8 @@ def test_fp8_expert_op_within_the_h_rounding_bound(oracle_mod):
             g, u = Wg[e] @ X[t], Wu[e] @ X[t]
             h = g / (1 + np.exp(-g)) * u
             y_exact += gates[t, j] * (Wd[e] @ h)
-            sb = np.repeat(np.max(np.abs(h).reshape(-1, 128), axis=1) / 448.0, 128)
+            spans = [(b0, min(f, b0 + 256)) for b0 in range(0, f, 256)]
+            sb = np.concatenate([np.full(b1 - b0, np.max(np.abs(h[b0:b1])) / 448.0) for b0, b1 in spans])
             bound += gates[t, j] * (np.abs(Wd[e]) @ (np.abs(h) * 2.0 ** -4 + sb * 2.0 ** -10))
         assert np.all(np.abs(y - y_exact) <= bound * 1.001 + 1e-12)
         # and the bound is far below the output's scale (the quantization is not vacuous)
