@@ -9,9 +9,9 @@
 // other byte off the memory path.
 //
 // A group is one slot (per-slot form) or one distinct expert with all of its tokens
-// (deduplicating form).  One call is one persistent kernel, one CTA per SM, 8 warps:
+// (deduplicating form).  One call is one persistent kernel, one CTA per SM, 10 warps:
 // warp 0 the TMA producer, warp 1 the tcgen05.mma issuer, warps 2-5 the epilogue (one TMEM
-// lane per thread), warps 6-7 the h formers.  Every CTA streams its share of two block
+// lane per thread), warps 6-9 the h formers.  Every CTA streams its share of two block
 // lists through one ring of shared-memory slots, without a break between them:
 //
 //   gate/up blocks.  A gate/up item is (group, 64-row tile of f); its block is one k slice:
@@ -28,9 +28,10 @@
 //   128-row block of d, tile): 128 rows of W_down by 64 columns (16 KB).  The blocks are
 //   again cut into equal ranges.  The producer moves on to them as soon as its gate/up
 //   blocks are issued, so the ring fills with W_down while the last gate/up sums are
-//   formed elsewhere.  An h former waits for the flags of the item's gate/up shares, forms
-//   h = silu(g) * u from their partial sums in a fixed order, as the bf16 B operand in its
-//   swizzled layout, and the epilogue adds gate * (W_down h) into the fp32 output with
+//   formed elsewhere.  The h formers wait for the flags of the item's gate/up shares and form
+//   h = silu(g) * u from their partial sums in a fixed order, as the B operand in its
+//   swizzled layout (a large group's tokens split over up to four warps, each a round of
+//   dependent L2 loads fewer), and the epilogue adds gate * (W_down h) into the fp32 output with
 //   atomics: the weighted combine and the reduction over f tiles are fused there.
 //
 // FP8 layers (e4m3 weights and x, one fp32 scale per weight row and per token) use the same
@@ -56,7 +57,9 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 256;                 // warps: producer, MMA, 4 epilogue, 2 h formers
+constexpr int kThreads = 320;                 // warps: producer, MMA, 4 epilogue, 4 h formers
+constexpr int kWarps = kThreads / 32;
+constexpr int kHWarps = kWarps - 6;           // h-former warps (6 ..)
 constexpr int kOB = 128;                      // d rows per down block
 constexpr int kNT = 16;                       // MMA N (token columns)
 constexpr uint32_t kWBytes = 16384;           // weight bytes of one block
@@ -87,12 +90,13 @@ constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
 // the grouping of the deduplicating form from ids: expert list, offsets, slot order, the count,
 // two scan scratch rows, then the per-expert counts (N <= 1024)
 constexpr uint32_t kGrpOff = kMiscOff + 16;
-constexpr uint32_t kGrpWords = 3 * kMaxFusedSlots + 1 + 1 + 16;
+constexpr uint32_t kGrpWords = 3 * kMaxFusedSlots + 1 + 1 + 2 * kWarps;
 constexpr uint32_t kCntOff = kGrpOff + ((kGrpWords * 4 + 15) & ~15u);
 constexpr uint32_t kSmem = kCntOff + 1024 * 4 + 1024;   // + alignment slack of the base
 static_assert(kSlotBytes % 1024 == 0 && kHOff % 1024 == 0 && kHEntry % 1024 == 0, "128-byte swizzle atoms");
 static_assert(kBarOff % 8 == 0, "mbarrier alignment");
 static_assert(kSmem <= 232448, "shared memory of one CTA");
+static_assert(4 * kThreads >= 1024 && kHWarps >= 1 && kHWarps <= kNT, "grouping bins, h-former warps");
 static_assert(kDnCol0 + 16 * kDownBufs <= kTmemCols, "TMEM columns");
 
 // Element type of a kernel instantiation: bf16 (kind::f16) or e4m3 (kind::f8f6f4).
@@ -285,17 +289,17 @@ __device__ void build_grouping(const ExpertArgs &a, int32_t *lst, int32_t *off, 
     }
     if (lane == 31) {
         scan[warp] = is;
-        scan[8 + warp] = in;
+        scan[kWarps + warp] = in;
     }
     __syncthreads();
     int es = is - cs, en = in - ne, tot_s = 0, tot_n = 0;
-    for (int w = 0; w < kThreads / 32; ++w) {
+    for (int w = 0; w < kWarps; ++w) {
         if (w < warp) {
             es += scan[w];
-            en += scan[8 + w];
+            en += scan[kWarps + w];
         }
         tot_s += scan[w];
-        tot_n += scan[8 + w];
+        tot_n += scan[kWarps + w];
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -376,7 +380,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             mbar_init(bar_dacc_empty + 8u * b, 4);      // the 4 epilogue warps
         }
         for (int b = 0; b < kHRing; ++b) {
-            mbar_init(bar_h_full + 8u * b, 1);          // the h-former warp of the run
+            mbar_init(bar_h_full + 8u * b, kHWarps);    // the run's leader for kHWarps - W + 1, each helper 1
             mbar_init(bar_h_empty + 8u * b, 1 + 4);     // the MMAs' commit and the epilogue warps
         }
         mbar_init(bar_drain, 1);
@@ -401,7 +405,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     // waits for another CTA's flag never holds an SM that CTA still needs.
     pdl_wait();
     pdl_trigger();
-    // The call's ticket, read by the warps that publish or wait for flags (2-7).  Once all of
+    // The call's ticket, read by the warps that publish or wait for flags (2 ..).  Once all of
     // them hold it, the CTA counts itself in; the last CTA of the grid to do so stores the
     // ticket as the new epoch, which no CTA of this call reads any more (each one read the
     // epoch before its count, and the acquire-release count orders that read before the
@@ -409,8 +413,8 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     uint32_t ticket = 0;
     if (warp >= 2) {
         ticket = call_ticket(a.sync);
-        named_barrier(1, 192);
-        if (warp == 7 && lane == 0 && atom_add_acq_rel_gpu(a.sync + 1, 1u) == gridDim.x - 1) {
+        named_barrier(1, kThreads - 64);
+        if (warp == kWarps - 1 && lane == 0 && atom_add_acq_rel_gpu(a.sync + 1, 1u) == gridDim.x - 1) {
             a.sync[1] = 0u;
             st_release_gpu(a.sync, ticket);
         }
@@ -707,7 +711,8 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             for (int t = 0; t < kNT; ++t) gt[t] = __uint_as_float(rec[1 + t]);
             if constexpr (F8) {
 #pragma unroll
-                for (int t = 0; t < kNT; ++t) gt[t] *= __uint_as_float(rec[17 + t]);   // h scale of the span
+                for (int t = 0; t < kNT; ++t)   // h scale of the span, written for the mask's tokens only
+                    if ((mask >> t) & 1u) gt[t] *= __uint_as_float(rec[17 + t]);
             }
             warp_arrive(bar_h_empty + 8u * hb);
             // e4m3: the W_down row scales of the next batch's units, loaded one batch ahead
@@ -768,21 +773,54 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         }
     } else {
         // ------------------------------------------------------------ h formers
-        // Warp 6 forms the even runs, warp 7 the odd ones, each up to kHRing runs ahead of the
-        // MMAs.  A lane holds 4 of the item's 128 f columns (c = lane + 32k: tile k / 2, row
-        // lane + 32 (k % 2)).  After the flags of the item's gate/up shares, h = silu(g) * u of
-        // each token from the partial sums, summed over the shares in order.
+        // The kHWarps warps take every run, up to kHRing runs ahead of the MMAs.  A run of a
+        // group of cnt slots is formed by W = min(kHWarps, ceil(cnt / E::TK)) of them, from the
+        // run's leader (warp run % kHWarps) on, the k-th token (ascending) by the (k % W)-th:
+        // one round of loads per warp for small groups, the rounds of a large group spread over
+        // the warps, and consecutive runs led by different warps.  The other warps skip the
+        // run: the leader arrives for them on h_full (kHWarps - W + 1 arrivals, each helper
+        // one), so none waits for a ring entry it does not fill.  W comes from the group's slot
+        // count, which the h formers copy to shared memory first (1 per group in the per-slot
+        // form), so a skipping warp reads nothing of the group.  A lane holds E::COLS of the
+        // item's columns (c = lane + 32 k: gate/up tile c / 64, row c % 64).  After the flags of
+        // the item's gate/up shares, h = silu(g) * u of each token from the partial sums, summed
+        // over the shares in order.
         const int hw = warp - 6;
+        // slot count of each group, clamped as group_tokens clamps the offsets (G <= N <= 1024;
+        // the count area of the in-kernel grouping is free once it is built)
+        int32_t *const gcnt = reinterpret_cast<int32_t *>(base_ptr + kCntOff);
+        if (ar.mode != kModePerSlot) {
+            const int S = a.n * a.m;
+            for (int g = hw * 32 + lane; g < G; g += kHWarps * 32)
+                gcnt[g] = max(0, min(S, ar.offsets[g + 1]) - max(0, ar.offsets[g]));
+            named_barrier(2, kHWarps * 32);
+        }
         uint32_t run = 0;
         for (long long b = dlo; b < dhi;) {
             const Seg sg = seg_at(ar, b, dhi, IB, T2);
             b = sg.b1;
             if (!sg.valid) continue;
             const uint32_t rr = run++;
-            if (static_cast<int>(rr & 1u) != hw) continue;
             const uint32_t hb = rr % kHRing, hph = (rr / kHRing) & 1u;
+            const int cnt = ar.mode == kModePerSlot ? 1 : gcnt[sg.g];
+            const int nw = min(kHWarps, max(1, (cnt + E::TK - 1) / E::TK));   // warps forming the run
+            const int first = (hw - static_cast<int>(rr % kHWarps) + kHWarps) % kHWarps;   // this warp's first token
+            if (first >= nw) continue;   // not a warp of this run
             GroupInfo gi;
             group_tokens(ar, sg.g, lane, gi);
+            // this warp's tokens: every nw-th of the group's, from its first
+            uint32_t mymask = gi.mask;
+            if (nw > 1) {
+                mymask = 0u;
+                int k = 0;
+#pragma unroll
+                for (int t = 0; t < kNT; ++t)
+                    if ((gi.mask >> t) & 1u) {
+                        if (k % nw == first) mymask |= 1u << t;
+                        ++k;
+                    }
+            }
+            const int mine = __popc(mymask);
             const int ntiles = min(E::ITEM, T - sg.tile * E::ITEM);   // real gate/up tiles of the item
             const int tile0 = sg.tile * E::ITEM;
             // the CTA shares of each real tile's gate/up item: first CTA and count
@@ -793,12 +831,14 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 p0[tl] = gsp.part_of(first);
                 span[tl] = min(gsp.part_of(first + KB - 1) - p0[tl] + 1, kMaxSpan);
             }
+            // a warp arrives for a run only after its entry is free, so no arrival runs ahead
             if (!warp_wait(bar_h_empty + 8u * hb, hph ^ 1u, abort_flag, a.err)) break;
             // the flags of the tiles' shares, 12 per tile (3 shares x 4 epilogue warps): flag
-            // l + 32 r waits in lane l, round r
+            // l + 32 r waits in lane l, round r; a warp with no token of the run waits for none
             bool flags_ok = true;
 #pragma unroll
             for (int r = 0; r < (E::ITEM * 12 + 31) / 32; ++r) {
+                if (mine == 0) break;
                 const int fi = lane + 32 * r, ftl = fi / 12, fsl = (fi % 12) / 4;
                 const uint32_t *fp = nullptr;
 #pragma unroll
@@ -808,20 +848,16 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             }
             if (!flags_ok) break;
             uint8_t *const hp = h_ptr + hb * kHEntry;
-            float hsc[kNT];             // e4m3: the run's h scale per token
-#pragma unroll
-            for (int t = 0; t < kNT; ++t) hsc[t] = 1.0f;
-            const int ntok = __popc(gi.mask);
-            // E::TK of the group's tokens at a time: all loads first (predicated, independent).
-            // Lane column k is c = lane + 32 k of the item: gate/up tile c / 64, row c % 64.
+            uint32_t *const rec = reinterpret_cast<uint32_t *>(info_ptr + hb * kInfoBytes);
+            // E::TK of this warp's tokens at a time: all loads first (predicated, independent)
 #pragma unroll
             for (int k0 = 0; k0 < kNT; k0 += E::TK) {
-                if (k0 >= ntok) break;
+                if (k0 >= mine) break;
                 uint32_t tk[E::TK];
                 int pk[E::TK];
 #pragma unroll
                 for (int j = 0; j < E::TK; ++j) {
-                    tk[j] = nth_token(gi.mask, k0 + j);
+                    tk[j] = nth_token(mymask, k0 + j);   // >= 16 past the last
                     pk[j] = 0;
 #pragma unroll
                     for (int t = 0; t < kNT; ++t) pk[j] = (tk[j] == static_cast<uint32_t>(t)) ? gi.pos[t] : pk[j];
@@ -870,8 +906,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
 #pragma unroll
                         for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
                         const float hs = mx > 0.0f ? mx / 448.0f : 1.0f;
-#pragma unroll
-                        for (int tt = 0; tt < kNT; ++tt) hsc[tt] = (t == static_cast<uint32_t>(tt)) ? hs : hsc[tt];
+                        if (lane == 0) rec[17 + t] = __float_as_uint(hs);   // the token's h scale
 #pragma unroll
                         for (int k = 0; k < E::COLS; ++k) {
                             const int c = lane + 32 * k, blk = c >> 7, fl = c & 127;   // block of 128, column in it
@@ -883,19 +918,16 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                     }
                 }
             }
-            if (lane == 0) {
-                uint32_t *const rec = reinterpret_cast<uint32_t *>(info_ptr + hb * kInfoBytes);
+            // the run's record (mask and gates) by the warp of its first token; the epilogue
+            // reads the h scales of the mask's tokens only
+            if (first == 0 && lane == 0) {
                 rec[0] = gi.mask;
 #pragma unroll
                 for (int t = 0; t < kNT; ++t) rec[1 + t] = __float_as_uint(gi.gt[t]);
-                if constexpr (F8) {
-#pragma unroll
-                    for (int t = 0; t < kNT; ++t) rec[17 + t] = __float_as_uint(hsc[t]);
-                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            warp_arrive(bar_h_full + 8u * hb);
+            warp_arrive_cnt(bar_h_full + 8u * hb, first == 0 ? static_cast<uint32_t>(kHWarps - nw + 1) : 1u);
         }
     }
 
