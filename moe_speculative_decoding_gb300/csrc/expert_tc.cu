@@ -88,15 +88,16 @@ constexpr uint32_t kBarOff = kSxOff + 4 * kNT * 4;
 constexpr int kNumBars = 2 * kStages + 2 * kGuBufs + 2 * kDownBufs + 2 * kHRing + 1;
 constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
 // the grouping of the deduplicating form from ids: expert list, offsets, slot order, the count,
-// two scan scratch rows, then the per-expert counts (N <= 1024)
+// two scan scratch rows, a copy of the ids, then the per-expert counts (N <= 1024)
 constexpr uint32_t kGrpOff = kMiscOff + 16;
-constexpr uint32_t kGrpWords = 3 * kMaxFusedSlots + 1 + 1 + 2 * kWarps;
+constexpr uint32_t kGrpWords = 3 * kMaxFusedSlots + 1 + 1 + 2 * kWarps + kMaxFusedSlots;
 constexpr uint32_t kCntOff = kGrpOff + ((kGrpWords * 4 + 15) & ~15u);
 constexpr uint32_t kSmem = kCntOff + 1024 * 4 + 1024;   // + alignment slack of the base
 static_assert(kSlotBytes % 1024 == 0 && kHOff % 1024 == 0 && kHEntry % 1024 == 0, "128-byte swizzle atoms");
 static_assert(kBarOff % 8 == 0, "mbarrier alignment");
 static_assert(kSmem <= 232448, "shared memory of one CTA");
-static_assert(4 * kThreads >= 1024 && kHWarps >= 1 && kHWarps <= kNT, "grouping bins, h-former warps");
+static_assert(4 * kThreads >= 1024 && kThreads >= kMaxFusedSlots && kHWarps >= 1 && kHWarps <= kNT,
+              "grouping bins and slots, h-former warps");
 static_assert(kDnCol0 + 16 * kDownBufs <= kTmemCols, "TMEM columns");
 
 // Element type of a kernel instantiation: bf16 (kind::f16) or e4m3 (kind::f8f6f4).
@@ -254,17 +255,18 @@ __device__ __forceinline__ uint32_t nth_token(uint32_t mask, int k) { return __f
 
 // The grouping of the deduplicating form (the counting sort of moe_group_slots): experts in
 // ascending order with their slot offsets, slots of an expert in ascending order; ids outside
-// [0, N) are left out of every group.  All threads of the CTA take part.
-__device__ void build_grouping(const ExpertArgs &a, int32_t *lst, int32_t *off, int32_t *ord, int32_t *cnt,
-                               int32_t *g_out, int32_t *scan) {
+// [0, N) are left out of every group.  All threads of the CTA take part; thread s holds the id
+// of slot s (S <= kMaxFusedSlots <= kThreads), loaded by the caller, and ids_s receives a copy.
+__device__ void build_grouping(const ExpertArgs &a, int my_id, int32_t *lst, int32_t *off, int32_t *ord,
+                               int32_t *cnt, int32_t *g_out, int32_t *scan, int32_t *ids_s) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int N = a.N, S = a.n * a.m;
     for (int i = tid; i < N; i += kThreads) cnt[i] = 0;
+    if (tid < S) ids_s[tid] = my_id;
     __syncthreads();
     bool bad = false;
-    for (int s = tid; s < S; s += kThreads) {
-        const int e = a.ids[s];
-        if (e >= 0 && e < N) atomicAdd(&cnt[e], 1);
+    if (tid < S) {
+        if (my_id >= 0 && my_id < N) atomicAdd(&cnt[my_id], 1);
         else bad = true;
     }
     if (__syncthreads_or(bad) && tid == 0 && blockIdx.x == 0) record_error(a.err, MOE_ERR_BAD_ID);
@@ -321,7 +323,7 @@ __device__ void build_grouping(const ExpertArgs &a, int32_t *lst, int32_t *off, 
     if (warp == 0) {
         for (int c0 = 0; c0 < S; c0 += 32) {
             const int s = c0 + lane;
-            const int e = s < S ? a.ids[s] : -1;
+            const int e = s < S ? ids_s[s] : -1;
             const bool v = e >= 0 && e < N;
             const uint32_t peers = __match_any_sync(kFull, v ? e : -2 - lane);
             const int rank = __popc(peers & ((1u << lane) - 1u));
@@ -405,19 +407,20 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     // waits for another CTA's flag never holds an SM that CTA still needs.
     pdl_wait();
     pdl_trigger();
+    // The deduplicating form from ids: thread s loads the id of slot s now, so that the load
+    // is in flight together with the epoch read below.
+    int my_id = -1;
+    if (a.mode == kModeDedupIds && static_cast<int>(threadIdx.x) < a.n * a.m) my_id = a.ids[threadIdx.x];
     // The call's ticket, read by the warps that publish or wait for flags (2 ..).  Once all of
-    // them hold it, the CTA counts itself in; the last CTA of the grid to do so stores the
-    // ticket as the new epoch, which no CTA of this call reads any more (each one read the
-    // epoch before its count, and the acquire-release count orders that read before the
-    // store).  The next call reads it after this grid is complete.
+    // them hold it, the CTA counts itself in (below, off the path to the first copies); the
+    // last CTA of the grid to do so stores the ticket as the new epoch, which no CTA of this
+    // call reads any more (each one read the epoch before its count, and the acquire-release
+    // count orders that read before the store).  The next call reads it after this grid is
+    // complete.
     uint32_t ticket = 0;
     if (warp >= 2) {
         ticket = call_ticket(a.sync);
         named_barrier(1, kThreads - 64);
-        if (warp == kWarps - 1 && lane == 0 && atom_add_acq_rel_gpu(a.sync + 1, 1u) == gridDim.x - 1) {
-            a.sync[1] = 0u;
-            st_release_gpu(a.sync, ticket);
-        }
     }
 
     // The routing every role reads: the call's, or, for the deduplicating form from ids, the
@@ -427,12 +430,18 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         int32_t *const grp = reinterpret_cast<int32_t *>(base_ptr + kGrpOff);
         int32_t *const lst = grp, *const off = grp + kMaxFusedSlots, *const ord = grp + 2 * kMaxFusedSlots + 1;
         int32_t *const gcount = grp + 3 * kMaxFusedSlots + 1, *const scan = gcount + 1;
-        build_grouping(a, lst, off, ord, reinterpret_cast<int32_t *>(base_ptr + kCntOff), gcount, scan);
+        int32_t *const ids_s = scan + 2 * kWarps;
+        build_grouping(a, my_id, lst, off, ord, reinterpret_cast<int32_t *>(base_ptr + kCntOff), gcount, scan, ids_s);
         ar.mode = kModeDedup;
         ar.expert_list = lst;
         ar.offsets = off;
         ar.slot_order = ord;
         ar.num_distinct = gcount;
+    }
+    // the CTA's count, after every warp of it read the epoch (the named barrier above)
+    if (warp == kWarps - 1 && lane == 0 && atom_add_acq_rel_gpu(a.sync + 1, 1u) == gridDim.x - 1) {
+        a.sync[1] = 0u;
+        st_release_gpu(a.sync, ticket);
     }
 
     using E = Elt<F8>;
