@@ -123,7 +123,7 @@ def _pool(seed, nodes, L, N, m):
 
 
 @pytest.mark.parametrize("nodes,L,N,m,S", [(18, 48, 128, 8, 20000), (10, 27, 64, 6, 1 << 10), (32, 4, 200, 5, 3000),
-                                           (0, 3, 64, 2, 1)])
+                                           (7, 9, 128, 4, 500), (0, 3, 64, 2, 1)])
 def test_union_cost_matches_oracle(nodes, L, N, m, S):
     bm, pv, bcoef = _pool(nodes * 7 + L, nodes, L, N, m)
     rng = np.random.default_rng(1)
@@ -138,5 +138,20 @@ def test_union_cost_matches_oracle(nodes, L, N, m, S):
     assert np.array_equal(out["F"].cpu().numpy(), ref["F"])
     assert np.array_equal(out["size"].cpu().numpy(), ref["size"])
     assert np.array_equal(out["R"].cpu().numpy(), ref["R"])
+    assert np.array_equal(out["T"].cpu().numpy(), ref["T"])
+    assert int(out["best"].item()) == ref["best"]
+
+def test_union_cost_negative_costs():
+    """Negative b coefficients make every T negative: the best is still the oracle's (its first
+    subset, then any strictly larger R/T)."""
+    bm, pv, bcoef = _pool(3, 9, 12, 128, 6)
+    bcoef = bcoef - 50.0
+    subsets = np.random.default_rng(2).integers(0, 1 << 9, size=700, dtype=np.uint64).astype(np.uint32)
+    ref = oracle.union_cost(bm, subsets, pv, bcoef, 0.01)
+    assert (ref["T"] < 0).all()
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    out = api.union_cost(t(bm.view(np.int64)), t(subsets.view(np.int32)), t(pv), t(bcoef), 0.01)
+    torch.cuda.synchronize()
+    assert np.array_equal(out["F"].cpu().numpy(), ref["F"])
     assert np.array_equal(out["T"].cpu().numpy(), ref["T"])
     assert int(out["best"].item()) == ref["best"]
