@@ -410,16 +410,20 @@ __global__ void __launch_bounds__(kSpecThreads) spec_accept_kernel(const SpecArg
 constexpr int kUcThreads = 256;
 constexpr int kUcPer = 1;
 constexpr int kUcChunk = 16;   // words of a subset's accumulator held in registers at a time
+constexpr int kUcTabChunk = 8;   // the same for the node-triple table
+constexpr int kUcMinBlocks = 5;  // CTAs per SM the registers must allow
 
 // 8-byte asynchronous copy global -> shared (no register staging, all in flight at once)
 __device__ __forceinline__ void cp_async8(void *smem_dst, const void *gsrc) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
 }
 
-__global__ void __launch_bounds__(kUcThreads) union_cost_kernel(const UnionArgs a, double *const blk_ratio,
-                                                               int *const blk_index) {
-    extern __shared__ uint64_t sbm[];   // [nodes+1][L][W]
-    const int words = (a.nodes + 1) * a.L * a.W;
+__global__ void __launch_bounds__(kUcThreads, kUcMinBlocks) union_cost_kernel(const UnionArgs a,
+                                                                             double *const blk_ratio,
+                                                                             int *const blk_index) {
+    // [nodes+1][L][W] bitmaps, or with the node-triple table only the root's row before it
+    extern __shared__ uint64_t sbm[];
+    const int words = (a.tab ? 1 : a.nodes + 1) * a.L * a.W;
     pdl_wait();
     pdl_trigger();
     for (int i = threadIdx.x; i < words; i += blockDim.x) cp_async8(sbm + i, a.bitmaps + i);
@@ -435,12 +439,80 @@ __global__ void __launch_bounds__(kUcThreads) union_cost_kernel(const UnionArgs 
         mask[k] = cs[k] < a.count ? a.subsets[cs[k]] & pool : 0u;
         f[k] = 0;
     }
+    const int LW = a.L * a.W;
+    int lw0 = 0;
+    if (a.tab) {
+        // Node triples: entry ((g * LW/2 + p) * 8 + c) holds word pair p of the OR of the nodes
+        // 3g+1..3g+3 selected by the bits of c (nodes past the pool count as empty), so the 8
+        // entries of one (triple, pair) fill 128 contiguous bytes and a warp's loads of them are
+        // conflict-free.  A lane then ORs one entry per triple, two triples per 3-input op.
+        const int NG = (a.nodes + 2) / 3, LW2 = LW >> 1;
+        uint4 *const tab = reinterpret_cast<uint4 *>(sbm + words);
+        for (int e = threadIdx.x; e < NG * LW2 * 8; e += blockDim.x) {
+            const int c = e & 7, gp = e >> 3, g = gp / LW2, pr = gp - g * LW2;
+            uint64_t w0 = 0, w1 = 0;
+#pragma unroll
+            for (int bb = 0; bb < 3; ++bb) {
+                const int v = 3 * g + 1 + bb;
+                if (v <= a.nodes && ((c >> bb) & 1)) {
+                    w0 |= __ldg(a.bitmaps + v * LW + 2 * pr);
+                    w1 |= __ldg(a.bitmaps + v * LW + 2 * pr + 1);
+                }
+            }
+            tab[e] = make_uint4(static_cast<uint32_t>(w0), static_cast<uint32_t>(w0 >> 32), static_cast<uint32_t>(w1),
+                                static_cast<uint32_t>(w1 >> 32));
+        }
+        __syncthreads();
+        for (int p0 = 0; p0 < LW2; p0 += kUcTabChunk / 2) {
+            const int np = min(kUcTabChunk / 2, LW2 - p0);
+            const uint4 *const r0 = reinterpret_cast<const uint4 *>(sbm) + p0;   // the root
+#pragma unroll
+            for (int k = 0; k < kUcPer; ++k) {
+                uint32_t acc[2 * kUcTabChunk];
+#pragma unroll
+                for (int j = 0; j < kUcTabChunk / 2; ++j) {
+                    const uint4 b = j < np ? r0[j] : make_uint4(0u, 0u, 0u, 0u);
+                    acc[4 * j] = b.x;
+                    acc[4 * j + 1] = b.y;
+                    acc[4 * j + 2] = b.z;
+                    acc[4 * j + 3] = b.w;
+                }
+                int g = 0;
+                for (; g + 1 < NG; g += 2) {
+                    const uint4 *const ta = tab + (g * LW2 + p0) * 8 + ((mask[k] >> (3 * g)) & 7u);
+                    const uint4 *const tb = tab + ((g + 1) * LW2 + p0) * 8 + ((mask[k] >> (3 * g + 3)) & 7u);
+#pragma unroll
+                    for (int j = 0; j < kUcTabChunk / 2; ++j) {
+                        if (j >= np) break;
+                        const uint4 x = ta[8 * j], y = tb[8 * j];
+                        acc[4 * j] |= x.x | y.x;
+                        acc[4 * j + 1] |= x.y | y.y;
+                        acc[4 * j + 2] |= x.z | y.z;
+                        acc[4 * j + 3] |= x.w | y.w;
+                    }
+                }
+                if (g < NG) {
+                    const uint4 *const ta = tab + (g * LW2 + p0) * 8 + ((mask[k] >> (3 * g)) & 7u);
+#pragma unroll
+                    for (int j = 0; j < kUcTabChunk / 2; ++j) {
+                        if (j >= np) break;
+                        const uint4 x = ta[8 * j];
+                        acc[4 * j] |= x.x;
+                        acc[4 * j + 1] |= x.y;
+                        acc[4 * j + 2] |= x.z;
+                        acc[4 * j + 3] |= x.w;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 2 * kUcTabChunk; ++j) f[k] += __popc(acc[j]);
+            }
+        }
+        lw0 = LW;
+    }
     // F(S) = popc of the OR of the root's and the selected nodes' bitmaps, per (layer, word).
     // The node loop is the same in every lane: all lanes read the same word (a broadcast, no
     // bank conflicts), and each ORs it into its subsets' accumulators under their subset bits.
-    const int LW = a.L * a.W;
-    int lw0 = 0;
-    if ((LW & 1) == 0) {
+    if (!a.tab && (LW & 1) == 0) {
         for (; lw0 + kUcChunk <= LW; lw0 += kUcChunk) {
             uint32_t acc[kUcPer][2 * kUcChunk];
             const uint4 *const r0 = reinterpret_cast<const uint4 *>(sbm + lw0);   // the root
@@ -616,7 +688,13 @@ cudaError_t launch_union_cost(const UnionArgs &a, void *scratch, cudaStream_t s,
     const int blocks = (a.count + 255) / 256;
     double *blk_ratio = static_cast<double *>(scratch);
     int *blk_index = reinterpret_cast<int *>(blk_ratio + blocks);
-    const size_t smem = static_cast<size_t>(a.nodes + 1) * a.L * a.W * sizeof(uint64_t);
+    // the node-triple table when the row width is even and it fits beside the bitmaps
+    UnionArgs b = a;
+    const size_t lw = static_cast<size_t>(a.L) * a.W;
+    const size_t bm_bytes = static_cast<size_t>(a.nodes + 1) * lw * sizeof(uint64_t);
+    const size_t tab_bytes = static_cast<size_t>((a.nodes + 2) / 3) * 8 * lw * sizeof(uint64_t);
+    b.tab = (lw % 2 == 0 && a.nodes > 0 && lw * sizeof(uint64_t) + tab_bytes <= kMaxUnionSmem) ? 1 : 0;
+    const size_t smem = b.tab ? lw * sizeof(uint64_t) + tab_bytes : bm_bytes;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(union_cost_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kMaxUnionSmem));
@@ -632,7 +710,7 @@ cudaError_t launch_union_cost(const UnionArgs &a, void *scratch, cudaStream_t s,
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, union_cost_kernel, a, blk_ratio, blk_index);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, union_cost_kernel, static_cast<const UnionArgs>(b), blk_ratio, blk_index);
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(1);
     cfg.blockDim = dim3(256);

@@ -37,6 +37,7 @@ struct UnionArgs {
     double *R, *T;
     int32_t *best;
     int nodes, L, W, count;
+    int tab;                   // set by launch_union_cost: the kernel uses the node-triple table
 };
 
 int spec_segment(int V);

@@ -123,8 +123,10 @@ def _pool(seed, nodes, L, N, m):
 
 
 @pytest.mark.parametrize("nodes,L,N,m,S", [(18, 48, 128, 8, 20000), (10, 27, 64, 6, 1 << 10), (32, 4, 200, 5, 3000),
-                                           (7, 9, 128, 4, 500), (0, 3, 64, 2, 1)])
+                                           (7, 9, 128, 4, 500), (12, 400, 128, 6, 800), (0, 3, 64, 2, 1)])
 def test_union_cost_matches_oracle(nodes, L, N, m, S):
+    # L*W even with the node-triple table (18/48, 32/4, 7/9), odd (10/27, 0/3), and even with a
+    # table too large for shared memory beside the bitmaps (12/400: the broadcast node loop)
     bm, pv, bcoef = _pool(nodes * 7 + L, nodes, L, N, m)
     rng = np.random.default_rng(1)
     if S == 1 << nodes:
