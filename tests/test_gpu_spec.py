@@ -45,8 +45,10 @@ def _gpu(draft, q, p, r, u, greedy=False):
     return na.cpu().numpy(), tok.cpu().numpy()
 
 
+# V % 4 = 0 runs the float4 loads (up to the largest vocabularies: 151936, 240000), the
+# other V the scalar loads
 @pytest.mark.parametrize("B,K,V", [(37, 5, 1000), (8, 0, 4097), (5, 31, 257), (16, 8, 32000), (3, 1, 1),
-                                   (16, 8, 151936), (64, 3, 7)])
+                                   (16, 8, 151936), (64, 3, 7), (3, 3, 240000)])
 def test_sampling_matches_oracle(B, K, V):
     draft, q, p, r, u = _case(B * 1000 + K * 10 + V % 97, B, K, V)
     na_o, tok_o = oracle.spec_accept(draft, q, p, r, u)
@@ -57,7 +59,7 @@ def test_sampling_matches_oracle(B, K, V):
         assert 0 < na_o.sum() < B * K or B < 4   # the cases exercise both outcomes
 
 
-@pytest.mark.parametrize("B,K,V", [(37, 5, 1000), (16, 8, 151936), (4, 31, 300), (6, 0, 50)])
+@pytest.mark.parametrize("B,K,V", [(37, 5, 1000), (16, 8, 151936), (4, 31, 300), (6, 0, 50), (3, 3, 240000)])
 def test_greedy_matches_oracle(B, K, V):
     draft, q, p, r, u = _case(7 + B + K, B, K, V)
     am = p.argmax(-1)
