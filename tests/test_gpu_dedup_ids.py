@@ -105,3 +105,38 @@ def test_routing_slices_need_only_element_alignment(oracle_mod):
     assert api.last_device_error(dl.ws) == 0
     for y in (ys, yd, yi):
         assert rel_max_err(y, ref) <= TOL_BF16
+
+
+def test_groups_larger_than_their_tokens_split_over_warps(oracle_mod):
+    """Two tokens naming one expert in all 8 slots: a group of 16 slots but 2 tokens, whose h is
+    formed by four h-former warps of which two hold no token, beside groups of 1 to 2 tokens;
+    bf16 and e4m3, against the oracle per token."""
+    d, f, N, m, n = 256, 256, 16, 8, 4
+    dl = DeviceLayer(d, f, N, m, "bf16", seed=750)
+    x = dl.activations(n, seed=751)
+    ids_np = np.array([[5] * 8, [5] * 8, list(range(8)), list(range(8, 16))], np.int32)
+    gates_np = np.random.default_rng(752).random((n, m)).astype(np.float32)
+    ids, gates = torch.from_numpy(ids_np).cuda(), torch.from_numpy(gates_np).cuda()
+    y1 = api.expert_op_dedup_ids(dl.layer, dl.w, x, ids, gates, ws=dl.ws).cpu().numpy()
+    assert api.last_device_error(dl.ws) == 0
+    ref = oracle_mod.expert_op_perslot(*dl.host(), synth.host_array(x), ids_np, gates_np)
+    assert rel_max_err(y1, ref) <= TOL_BF16
+    grp = api.group_slots(ids, N, ws=dl.ws)
+    y2 = api.expert_op_dedup(dl.layer, dl.w, x, gates, grp, ws=dl.ws).cpu().numpy()
+    assert rel_max_err(y1, y2) <= 1e-4
+    # e4m3: the same grouping on the FP8 kernel (TK = 2 tokens per round: four warps as well)
+    l8 = api.make_layer(d, f, N, m, "e4m3")
+    ws8 = api.workspace(l8, 16, "cuda")
+    w8, sc = api.quantize_experts(dl.w)
+    xq, sx = api.quantize_rows_e4m3(x)
+    y8 = api.expert_op_dedup_ids_fp8(l8, w8, sc, xq, sx, ids, gates, ws=ws8).cpu().numpy()
+    assert api.last_device_error(ws8) == 0
+    xq_h, sx_h = xq.cpu().numpy(), sx.cpu().numpy()
+    for t in range(n):
+        idx = torch.as_tensor(ids_np[t].astype(np.int64), device="cuda")
+        cg, cu, cd = (w.index_select(0, idx).cpu().numpy() for w in w8)
+        sg, su, sd = (s.index_select(0, idx).cpu().numpy() for s in sc)
+        local = np.arange(m, dtype=np.int32)[None, :].repeat(n, axis=0)
+        y_ref = oracle_mod.expert_op_token_fp8(cg, cu, cd, sg, su, sd, xq_h, sx_h, local,
+                                               gates_np.astype(np.float64), t)
+        assert np.max(np.abs(y8[t] - y_ref)) <= TOL_BF16 * np.sqrt(np.mean(y_ref ** 2)), t
