@@ -257,6 +257,8 @@ __device__ __forceinline__ uint32_t nth_token(uint32_t mask, int k) { return __f
 // ascending order with their slot offsets, slots of an expert in ascending order; ids outside
 // [0, N) are left out of every group.  All threads of the CTA take part; thread s holds the id
 // of slot s (S <= kMaxFusedSlots <= kThreads), loaded by the caller, and ids_s receives a copy.
+// On return the expert list, offsets and count are visible to every thread, the slot order to
+// warps 2 and up.
 __device__ void build_grouping(const ExpertArgs &a, int my_id, int32_t *lst, int32_t *off, int32_t *ord,
                                int32_t *cnt, int32_t *g_out, int32_t *scan, int32_t *ids_s) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -319,8 +321,10 @@ __device__ void build_grouping(const ExpertArgs &a, int my_id, int32_t *lst, int
         off[tot_n] = tot_s;
     }
     __syncthreads();
-    // stable scatter of the slots, 32 at a time in ascending order, by one warp
-    if (warp == 0) {
+    // Stable scatter of the slots, 32 at a time in ascending order, by the first h-former warp.
+    // Only the epilogue and the h formers read the slot order (warps 2 ..), so the producer and
+    // the MMA warp go on with the expert list and the offsets.
+    if (warp == 6) {
         for (int c0 = 0; c0 < S; c0 += 32) {
             const int s = c0 + lane;
             const int e = s < S ? ids_s[s] : -1;
@@ -334,7 +338,7 @@ __device__ void build_grouping(const ExpertArgs &a, int my_id, int32_t *lst, int
             __syncwarp();
         }
     }
-    __syncthreads();
+    if (warp >= 2) named_barrier(3, kThreads - 64);
 }
 
 // ==================================================================== the kernel
