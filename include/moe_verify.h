@@ -81,6 +81,8 @@ typedef struct {
 
 /* Largest pass size (tokens per verification pass) the expert operation accepts. */
 #define MOE_MAX_PASS_TOKENS 16
+/* The per-slot calls take passes of up to 64 tokens, as consecutive launches of up to 16. */
+#define MOE_MAX_PERSLOT_TOKENS 64
 
 /* Returns MOE_ABI_VERSION. */
 int32_t moe_abi_version(void);
@@ -155,8 +157,11 @@ moe_status_t moe_group_slots(const int32_t *ids, int32_t n, int32_t m, int32_t N
  *   ids   [dev] int32 [n, m];  gates [dev] fp32 [n, m].
  *   y     [dev] fp32 [n, d]    accumulate == 0: y is overwritten; != 0: added to.
  *   ws    [dev] workspace of ws_bytes >= moe_workspace_bytes(layer, n).
- * Supported: 1 <= n <= MOE_MAX_PASS_TOKENS.  Summation order inside y is not fixed
- * (results may differ in the last bits between runs).
+ * Supported: 1 <= n <= MOE_MAX_PERSLOT_TOKENS.  A pass above MOE_MAX_PASS_TOKENS runs as
+ * consecutive launches of up to MOE_MAX_PASS_TOKENS tokens on s (the per-slot form reads
+ * every slot's expert either way; the launches write disjoint rows of y and share ws, which
+ * needs only moe_workspace_bytes(layer, MOE_MAX_PASS_TOKENS)).  Summation order inside y is
+ * not fixed (results may differ in the last bits between runs).
  */
 moe_status_t moe_expert_op_perslot(const moe_layer_t *layer, const void *w_gate, const void *w_up,
                                    const void *w_down, const void *x, const int32_t *ids,

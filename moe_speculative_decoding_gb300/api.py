@@ -18,7 +18,8 @@ from . import build as _build
 
 MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
 MOE_FLAG_SIMT = 1
-MAX_PASS_TOKENS = 16
+MAX_PASS_TOKENS = 16        # tokens per launch of the expert kernel
+MAX_PERSLOT_TOKENS = 64     # tokens per per-slot call (consecutive launches of up to 16)
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_BAD_ID", 6: "MOE_ERR_DEVICE_TIMEOUT"}
 

@@ -124,6 +124,11 @@ moe_status_t run_expert(const moe_layer_t *L, const ExpertArgs &a, int max_group
 
 }  // namespace
 
+namespace {
+// Element size of a layer's activations (bf16, fp32 or e4m3).
+size_t x_elt_bytes(const moe_layer_t *L) { return L->x_dtype == MOE_BF16 ? 2u : (L->x_dtype == MOE_E4M3 ? 1u : 4u); }
+}  // namespace
+
 extern "C" {
 
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
@@ -185,6 +190,22 @@ moe_status_t moe_expert_op_perslot(const moe_layer_t *layer, const void *w_gate,
                                    const void *w_down, const void *x, const int32_t *ids, const float *gates,
                                    int32_t n, int32_t accumulate, float *y, void *ws, size_t ws_bytes,
                                    moe_stream_t s) {
+    if (n > MOE_MAX_PASS_TOKENS && n <= MOE_MAX_PERSLOT_TOKENS) {
+        // consecutive launches of up to MOE_MAX_PASS_TOKENS tokens (each validates its part)
+        moe_status_t st = check_layer(layer);
+        if (st != MOE_OK) return st;
+        if (x == nullptr || ids == nullptr || gates == nullptr || y == nullptr) return MOE_ERR_ARG;
+        const size_t xrow = static_cast<size_t>(layer->d) * x_elt_bytes(layer);
+        for (int32_t t0 = 0; t0 < n; t0 += MOE_MAX_PASS_TOKENS) {
+            const int32_t nc = n - t0 < MOE_MAX_PASS_TOKENS ? n - t0 : MOE_MAX_PASS_TOKENS;
+            const size_t so = static_cast<size_t>(t0) * layer->m;
+            st = moe_expert_op_perslot(layer, w_gate, w_up, w_down, static_cast<const uint8_t *>(x) + t0 * xrow,
+                                       ids + so, gates + so, nc, accumulate, y + static_cast<size_t>(t0) * layer->d,
+                                       ws, ws_bytes, s);
+            if (st != MOE_OK) return st;
+        }
+        return MOE_OK;
+    }
     moe_status_t st = check_expert_common(layer, w_gate, w_up, w_down, x, gates, n, y, ws, ws_bytes);
     if (st != MOE_OK) return st;
     if (is_fp8(layer)) return MOE_ERR_UNSUPPORTED;   // e4m3 needs its scales: the _fp8 call
@@ -240,6 +261,23 @@ moe_status_t moe_expert_op_perslot_fp8(const moe_layer_t *layer, const void *w_g
                                        const void *w_down, const moe_weight_scales_t *scales, const void *x,
                                        const float *x_scale, const int32_t *ids, const float *gates, int32_t n,
                                        int32_t accumulate, float *y, void *ws, size_t ws_bytes, moe_stream_t s) {
+    if (n > MOE_MAX_PASS_TOKENS && n <= MOE_MAX_PERSLOT_TOKENS) {
+        // consecutive launches of up to MOE_MAX_PASS_TOKENS tokens (each validates its part)
+        moe_status_t st = check_layer(layer);
+        if (st != MOE_OK) return st;
+        if (x == nullptr || x_scale == nullptr || ids == nullptr || gates == nullptr || y == nullptr) return MOE_ERR_ARG;
+        const size_t xrow = static_cast<size_t>(layer->d) * x_elt_bytes(layer);
+        for (int32_t t0 = 0; t0 < n; t0 += MOE_MAX_PASS_TOKENS) {
+            const int32_t nc = n - t0 < MOE_MAX_PASS_TOKENS ? n - t0 : MOE_MAX_PASS_TOKENS;
+            const size_t so = static_cast<size_t>(t0) * layer->m;
+            st = moe_expert_op_perslot_fp8(layer, w_gate, w_up, w_down, scales,
+                                           static_cast<const uint8_t *>(x) + t0 * xrow, x_scale + t0, ids + so,
+                                           gates + so, nc, accumulate, y + static_cast<size_t>(t0) * layer->d, ws,
+                                           ws_bytes, s);
+            if (st != MOE_OK) return st;
+        }
+        return MOE_OK;
+    }
     moe_status_t st = check_expert_common(layer, w_gate, w_up, w_down, x, gates, n, y, ws, ws_bytes);
     if (st != MOE_OK) return st;
     if (!is_fp8(layer)) return MOE_ERR_UNSUPPORTED;

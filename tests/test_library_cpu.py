@@ -50,8 +50,12 @@ def test_argument_validation_before_any_launch(lib):
     bad = api.make_layer(2048, 700, 128, 8)   # f not a multiple of 64
     args = [None] * 6
     assert lib.moe_expert_op_perslot(ctypes.byref(bad), *args, 4, 0, None, None, 0, None) == 2
-    # n above the pass limit
-    assert lib.moe_expert_op_perslot(ctypes.byref(L), *args, 17, 0, None, None, 0, None) == 2
+    # n above the per-slot limit (64); 17..64 are taken as launches of up to 16 tokens, so here
+    # their null pointers are the error; the deduplicating form stops at 16
+    assert lib.moe_expert_op_perslot(ctypes.byref(L), *args, 65, 0, None, None, 0, None) == 2
+    assert lib.moe_expert_op_perslot(ctypes.byref(L), *args, 17, 0, None, None, 0, None) == 1
+    assert lib.moe_expert_op_perslot(ctypes.byref(L), *args, 64, 0, None, None, 0, None) == 1
+    assert lib.moe_expert_op_dedup_ids(ctypes.byref(L), *args, 17, 0, None, None, 0, None) == 2
     # null pointers
     assert lib.moe_expert_op_perslot(ctypes.byref(L), *args, 4, 0, None, None, 0, None) == 1
     mixed = api.Layer(2048, 768, 128, 8, 1, 0, 0)   # bf16 weights with fp32 x
