@@ -160,8 +160,10 @@ moe_status_t moe_group_slots(const int32_t *ids, int32_t n, int32_t m, int32_t N
  * Supported: 1 <= n <= MOE_MAX_PERSLOT_TOKENS.  A pass above MOE_MAX_PASS_TOKENS runs as
  * consecutive launches of up to MOE_MAX_PASS_TOKENS tokens on s (the per-slot form reads
  * every slot's expert either way; the launches write disjoint rows of y and share ws, which
- * needs only moe_workspace_bytes(layer, MOE_MAX_PASS_TOKENS)).  Summation order inside y is
- * not fixed (results may differ in the last bits between runs).
+ * needs only moe_workspace_bytes(layer, MOE_MAX_PASS_TOKENS)).  Each launch is validated
+ * before it is enqueued and the first error ends the call; the chunks share the layer and
+ * the pointers' alignment, so an argument error is found before the first launch.
+ * Summation order inside y is not fixed (results may differ in the last bits between runs).
  */
 moe_status_t moe_expert_op_perslot(const moe_layer_t *layer, const void *w_gate, const void *w_up,
                                    const void *w_down, const void *x, const int32_t *ids,
