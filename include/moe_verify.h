@@ -84,10 +84,11 @@ typedef struct {
 /* The per-slot calls take passes of up to 64 tokens, as consecutive launches of up to 16. */
 #define MOE_MAX_PERSLOT_TOKENS 64
 
-/* Returns MOE_ABI_VERSION. */
+/* Returns MOE_ABI_VERSION.  Library infrastructure: no passage of the pages defines it. */
 int32_t moe_abi_version(void);
 
-/* Static description of a status code (never NULL). */
+/* Static description of a status code (never NULL).  Library infrastructure: no passage of the
+ * pages defines it. */
 const char *moe_status_str(moe_status_t status);
 
 /*
@@ -105,7 +106,8 @@ const char *moe_status_str(moe_status_t status);
  */
 size_t moe_workspace_bytes(const moe_layer_t *layer, int32_t n_max);
 
-/* Zeroes all ws_bytes of the workspace [dev] on stream s. */
+/* Zeroes all ws_bytes of the workspace [dev] on stream s.  Library infrastructure: no passage of
+ * the pages defines it. */
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t s);
 
 /*
@@ -422,12 +424,15 @@ moe_status_t moe_fit_op_times(int32_t count, const int32_t *n, const int32_t *U,
 
 /*
  * Synchronises stream s, reads the device error word of the workspace [dev] into *code
- * (a moe_status_t value; MOE_OK if nothing was recorded) and clears it.
+ * (a moe_status_t value; MOE_OK if nothing was recorded) and clears it.  Library
+ * infrastructure: no passage of the pages defines it.
  */
 moe_status_t moe_last_device_error(void *ws, moe_stream_t s, int32_t *code);
 
 /*
- * Measurement helper, not part of the method: a read-only streaming probe.  One CTA per SM
+ * Measurement helper, not part of the method: a read-only streaming probe, the read side of the
+ * bandwidth the expert operation is measured against ([Lan] §2 "Effective bandwidth": requested
+ * bytes over time, against the memory's bandwidth).  One CTA per SM
  * streams its contiguous share of buf through 1-D TMA bulk copies into shared memory and
  * discards it: floor(bytes / 32768) * 32768 bytes are read.  Time it on the stream to get the
  * read bandwidth the expert kernel's weight stream can reach, beside a copy's (read + write).
