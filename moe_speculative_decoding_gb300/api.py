@@ -76,6 +76,7 @@ _lib = None
 
 
 def lib_path() -> str:
+    """Path of the in-tree libmoeverify.so (library infrastructure)."""
     return _build.LIB
 
 
@@ -157,11 +158,13 @@ def _dev(t: torch.Tensor, name: str, dtype=None, shape=None):
 # ---------------------------------------------------------------- layer + workspace
 
 def make_layer(d: int, f: int, N: int, m: int, dtype: str = "bf16", simt: bool = False) -> Layer:
+    """A moe_layer_t: hidden size d, expert size f, N experts, top-m, weight/activation dtype ([Lan] §1: the expert operation's shapes)."""
     code = {"bf16": MOE_BF16, "f32": MOE_F32, "e4m3": MOE_E4M3}[dtype]
     return Layer(d, f, N, m, code, code, MOE_FLAG_SIMT if simt else 0)
 
 
 def workspace(layer: Layer, n_max: int = MAX_PASS_TOKENS, device=None) -> torch.Tensor:
+    """A zeroed device workspace for passes of up to n_max tokens (moe_workspace_bytes, moe_workspace_init; infrastructure)."""
     nbytes = int(lib().moe_workspace_bytes(ctypes.byref(layer), n_max))
     ws = torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
     _check(lib().moe_workspace_init(ctypes.c_void_p(ws.data_ptr()), nbytes, _stream(ws.device)),
@@ -170,6 +173,7 @@ def workspace(layer: Layer, n_max: int = MAX_PASS_TOKENS, device=None) -> torch.
 
 
 def last_device_error(ws: torch.Tensor) -> int:
+    """moe_last_device_error: synchronise, return and clear the workspace's device error code (infrastructure)."""
     code = ctypes.c_int32(0)
     _check(lib().moe_last_device_error(ctypes.c_void_p(ws.data_ptr()), _stream(ws.device),
                                        ctypes.byref(code)), "moe_last_device_error")
@@ -207,6 +211,7 @@ class Grouping:
 
 
 def group_slots(ids: torch.Tensor, N: int, out: Grouping | None = None, ws=None) -> Grouping:
+    """moe_group_slots: the pass's slots grouped by expert, a counting sort ([Lan] §1, App. E): U, expert list, offsets, slot order."""
     n, m = ids.shape
     g = out or Grouping.empty(n, m, N, ids.device)
     _check(lib().moe_group_slots(_dev(ids, "ids", torch.int32), n, m, N,
@@ -234,6 +239,7 @@ def _y(layer, x, y):
 
 def expert_op_perslot(layer: Layer, weights, x: torch.Tensor, ids: torch.Tensor, gates: torch.Tensor,
                       y=None, accumulate: bool = False, ws=None):
+    """moe_expert_op_perslot: the per-slot form of the expert operation, one expert read per slot ([Lan] §1)."""
     n = x.shape[0]
     ws = ws if ws is not None else workspace(layer, n, x.device)
     y, yp = _y(layer, x, y)
@@ -263,6 +269,7 @@ def expert_op_dedup_ids(layer: Layer, weights, x: torch.Tensor, ids: torch.Tenso
 
 def expert_op_dedup(layer: Layer, weights, x: torch.Tensor, gates: torch.Tensor, grouping: Grouping,
                     y=None, accumulate: bool = False, ws=None):
+    """moe_expert_op_dedup: the deduplicating form on a precomputed grouping, each distinct expert read once ([Lan] §1)."""
     n = x.shape[0]
     ws = ws if ws is not None else workspace(layer, n, x.device)
     y, yp = _y(layer, x, y)
@@ -281,6 +288,7 @@ def expert_op_dedup(layer: Layer, weights, x: torch.Tensor, gates: torch.Tensor,
 # ---------------------------------------------------------------- host-side report
 
 def pass_bytes(layer: Layer, ids_host) -> dict:
+    """moe_pass_bytes: E_slot = n m w, E_dedup = U w and u-bar of one pass, on the host ([Lan] §1 "Bytes", §2 "Effective bandwidth")."""
     ids = np.ascontiguousarray(np.asarray(ids_host, dtype=np.int32))
     n = ids.shape[0] if ids.ndim == 2 else ids.size // layer.m
     out = _PassBytes()
@@ -291,6 +299,7 @@ def pass_bytes(layer: Layer, ids_host) -> dict:
 
 
 def bandwidth_report(n_lo: int, slot_bytes, dedup_bytes, t_slot, t_dedup) -> dict:
+    """moe_bandwidth_report: u-bar(n), beta_p, r(n), S(n) and the crossover from bytes and times ([Lan] §2 "Effective bandwidth", §3.1, §2 "Testing the inputs")."""
     arrs = [np.ascontiguousarray(np.asarray(a, dtype=np.float64)) for a in
             (slot_bytes, dedup_bytes, t_slot, t_dedup)]
     count = arrs[0].size
@@ -305,10 +314,12 @@ def bandwidth_report(n_lo: int, slot_bytes, dedup_bytes, t_slot, t_dedup) -> dic
 
 
 def expected_union(N: int, m: int, n: int) -> float:
+    """moe_expected_union: E[U] = N (1 - q^n) under uniform routing ([Lan] §1)."""
     return float(lib().moe_expected_union(N, m, n))
 
 
 def best_draft_length(V, a: float) -> int:
+    """moe_best_draft_length: the smallest maximiser k* of G_a(k) / V(k) ([Lan] §1 "Speculative decoding")."""
     V = np.ascontiguousarray(np.asarray(V, dtype=np.float64))
     k = int(lib().moe_best_draft_length(ctypes.c_void_p(V.ctypes.data), V.size - 1, float(a)))
     if k < 0:
@@ -336,27 +347,32 @@ def staircase(V) -> dict:
 
 
 def speedup(V, k: int, a: float) -> float:
+    """moe_speedup: T_a(k) / T_a(0) = G_a(k) V(0) / V(k), the speed-up of draft length k ([Lan] §3.2 (9))."""
     V = _times(V)
     return float(lib().moe_speedup(ctypes.c_void_p(V.ctypes.data), V.size - 1, int(k), float(a)))
 
 
 def reuse_threshold(k: int, a: float, mW: float, B_k: float, beta_1: float, tau_1: float,
                     dD_over_betaD: float = 0.0, dphi: float = 0.0) -> float:
+    """moe_reuse_threshold: the deduplicating engine's reuse threshold rho*_k(a) in time ([Lan] §3.4 (14), App. B.2 (B.12)-(B.14))."""
     t = ThresholdIn(mW, B_k, beta_1, tau_1, dD_over_betaD, dphi)
     return float(lib().moe_reuse_threshold(int(k), float(a), ctypes.byref(t)))
 
 
 def reuse_threshold_bytes(k: int, a: float, mW: float, D_1: float = 0.0, D_k1: float = 0.0) -> float:
+    """moe_reuse_threshold_bytes: the same threshold with one bandwidth and no fixed time ([Lan] §3.4 (16), (B.16))."""
     return float(lib().moe_reuse_threshold_bytes(int(k), float(a), float(mW), float(D_1), float(D_k1)))
 
 
 def error_bounds(eps: float) -> dict:
+    """moe_error_bounds: delta, the verify factor of (17)-(18) and the decision margin for a relative bandwidth error eps ([Lan] §3.5, Table 2, App. C)."""
     out = _ErrorBounds()
     _check(lib().moe_error_bounds(float(eps), ctypes.byref(out)), "moe_error_bounds")
     return {f: getattr(out, f) for f, _ in _ErrorBounds._fields_}
 
 
 def kstar_separated(V, a: float, delta: float) -> bool:
+    """moe_kstar_separated: the separation condition of (20), under which the predicted k* is the true one ([Lan] §3.5, Table 2)."""
     V = _times(V)
     r = int(lib().moe_kstar_separated(ctypes.c_void_p(V.ctypes.data), V.size - 1, float(a), float(delta)))
     if r < 0:
@@ -408,6 +424,7 @@ def _scales(layer: Layer, scales) -> WeightScales:
 
 def expert_op_perslot_fp8(layer: Layer, weights, scales, xq: torch.Tensor, x_scale: torch.Tensor, ids: torch.Tensor,
                           gates: torch.Tensor, y=None, accumulate: bool = False, ws=None):
+    """moe_expert_op_perslot_fp8: the per-slot form on e4m3 experts with row scales (the quantized experts of [Lan] App. E Table 6)."""
     n = xq.shape[0]
     ws = ws if ws is not None else workspace(layer, n, xq.device)
     y, yp = _y(layer, xq, y)
@@ -424,6 +441,7 @@ def expert_op_perslot_fp8(layer: Layer, weights, scales, xq: torch.Tensor, x_sca
 
 def expert_op_dedup_ids_fp8(layer: Layer, weights, scales, xq: torch.Tensor, x_scale: torch.Tensor, ids: torch.Tensor,
                             gates: torch.Tensor, y=None, accumulate: bool = False, ws=None):
+    """moe_expert_op_dedup_ids_fp8: the deduplicating form from ids on e4m3 experts, the grouping built in the kernel ([Lan] §1; App. E Table 6)."""
     n = xq.shape[0]
     ws = ws if ws is not None else workspace(layer, n, xq.device)
     y, yp = _y(layer, xq, y)
@@ -440,6 +458,7 @@ def expert_op_dedup_ids_fp8(layer: Layer, weights, scales, xq: torch.Tensor, x_s
 
 def expert_op_dedup_fp8(layer: Layer, weights, scales, xq: torch.Tensor, x_scale: torch.Tensor, gates: torch.Tensor,
                         grouping: Grouping, y=None, accumulate: bool = False, ws=None):
+    """moe_expert_op_dedup_fp8: the deduplicating form on e4m3 experts and a precomputed grouping ([Lan] §1; App. E Table 6)."""
     n = xq.shape[0]
     ws = ws if ws is not None else workspace(layer, n, xq.device)
     y, yp = _y(layer, xq, y)
