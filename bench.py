@@ -422,7 +422,8 @@ def verify_side_leg(device, reps: int = 20, B: int = 16, K: int = 8, V: int = 15
     torch.cuda.synchronize(device)
     t = ev[0].elapsed_time(ev[1]) * 1e-3 / reps
     out["union_cost"] = dict(subsets=S, nodes=nodes, layers=layers, experts=N, us_per_call=round(t * 1e6, 2),
-                             subsets_per_s=round(S / t, 1), best=int(res["best"].item()), bound="alu")
+                             subsets_per_s=round(S / t, 1), best=int(res["best"].item()),
+                             **union_roofline(nodes, layers, W, S, t, torch.cuda.get_device_properties(device).multi_processor_count))
     out["config"] = dict(B=B, K=K, V=V, input_sets=sets, reps=reps, timing="CUDA-graph replays of one call per input set")
     return out
 
@@ -490,6 +491,30 @@ def fit_leg(wl, weights, device, reps: int = 7, windows: int = 8, n_max: int = 1
                            c_t_us_per_token=round(dedup[2] * 1e6, 4), union_tbps=round(1e-12 / dedup[1], 3)),
                 eps_slot=round(eps_s, 4), eps_dedup=round(eps_d, 4), eps=round(max(eps_s, eps_d), 4),
                 scored_windows=len(err_s))
+
+
+UNION_SMEM_MAX = 200 * 1024       # shared memory the union-cost kernel may use (its table path's limit)
+SMEM_BYTES_PER_CLK = 128          # shared memory delivered to the lanes per clock and SM (32 banks x 4 B)
+SM_MAX_CLOCK_HZ = 2.07e9          # GB300's maximum SM clock
+
+
+def union_roofline(nodes, layers, W, S, t, sms):
+    """The union-cost kernel's roofline: the bytes its lanes read from shared memory per call (with
+    the node-triple table, one 8-byte word per triple and the root per (layer, word) and subset;
+    otherwise one per node and the root) over what the SMs' shared memory delivers at the maximum
+    clock.  The kernel takes the table path under the same rule as here."""
+    lw = layers * W
+    ngroups = (nodes + 2) // 3
+    table = lw % 2 == 0 and nodes > 0 and lw * 8 + ngroups * 8 * lw * 8 <= UNION_SMEM_MAX
+    words = (ngroups + 1 if table else nodes + 1) * lw
+    delivered = S * words * 8
+    peak = sms * SMEM_BYTES_PER_CLK * SM_MAX_CLOCK_HZ
+    achieved = delivered / t
+    return dict(bound="shared-memory delivery", path="node-triple table" if table else "broadcast node loop",
+                delivered_bytes_per_call=int(delivered), achieved_tbps=round(achieved / 1e12, 2),
+                peak_tbps=round(peak / 1e12, 2), frac=round(achieved / peak, 4),
+                peak_source="152 SMs x 128 B per clock x 2.07 GHz (derived)" if sms == 152 else
+                f"{sms} SMs x 128 B per clock x 2.07 GHz (derived)")
 
 
 def kernel_traffic(kernel: str):
