@@ -218,7 +218,9 @@ moe_status_t moe_expert_op_dedup_ids(const moe_layer_t *layer, const void *w_gat
  *   MOE_ERR_BAD_ID or MOE_ERR_DEVICE_TIMEOUT), written on stream s after the kernels.
  * Scratch: a 16 MiB array inside the library, held by every GPU that loads it until the
  * process exits.  A layer or pass whose workspace (moe_workspace_bytes) would exceed it is
- * rejected with MOE_ERR_WORKSPACE.  Its error word is cleared at the start of every call,
+ * rejected with MOE_ERR_WORKSPACE.  Every argument is checked first (the same checks and
+ * statuses as moe_expert_op_perslot): a rejected call enqueues no device work.  Its error
+ * word is cleared at the start of every call,
  * and the array keeps the last call's contents after it.  All calls on a GPU share it, so calls that
  * overlap on that GPU (on different streams, or from different host threads) race: order
  * them on one stream.

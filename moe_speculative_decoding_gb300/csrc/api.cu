@@ -124,6 +124,27 @@ moe_status_t run_expert(const moe_layer_t *L, const ExpertArgs &a, int max_group
 
 }  // namespace
 
+namespace moe {
+// The host checks of moe_expert_op_perslot that do not involve the workspace: the status it
+// returns before any device work for these arguments (MOE_OK when they pass).
+moe_status_t check_perslot_call(const moe_layer_t *L, const void *wg, const void *wu, const void *wd, const void *x,
+                                const int32_t *ids, const float *gates, int32_t n, const float *y) {
+    const moe_status_t st = check_layer(L);
+    if (st != MOE_OK) return st;
+    if (n < 1) return MOE_ERR_ARG;
+    if (n > MOE_MAX_PERSLOT_TOKENS) return MOE_ERR_UNSUPPORTED;
+    const void *ptrs[] = {wg, wu, wd, x, y};
+    for (const void *p : ptrs)
+        if (p == nullptr || !aligned16(p)) return MOE_ERR_ARG;
+    if (gates == nullptr || !aligned4(gates) || ids == nullptr || !aligned4(ids)) return MOE_ERR_ARG;
+    if (is_fp8(L)) return MOE_ERR_UNSUPPORTED;   // e4m3 needs its scales: the _fp8 call
+    return MOE_OK;
+}
+
+// The layer runs on the tensor-core path, whose workspace holds flags and partial sums.
+bool layer_uses_tc(const moe_layer_t *L) { return check_layer(L) == MOE_OK && uses_tc(L); }
+}  // namespace moe
+
 namespace {
 // Element size of a layer's activations (bf16, fp32 or e4m3).
 size_t x_elt_bytes(const moe_layer_t *L) { return L->x_dtype == MOE_BF16 ? 2u : (L->x_dtype == MOE_E4M3 ? 1u : 4u); }
@@ -190,6 +211,8 @@ moe_status_t moe_expert_op_perslot(const moe_layer_t *layer, const void *w_gate,
                                    const void *w_down, const void *x, const int32_t *ids, const float *gates,
                                    int32_t n, int32_t accumulate, float *y, void *ws, size_t ws_bytes,
                                    moe_stream_t s) {
+    moe_status_t st0 = check_perslot_call(layer, w_gate, w_up, w_down, x, ids, gates, n, y);
+    if (st0 != MOE_OK) return st0;
     if (n > MOE_MAX_PASS_TOKENS && n <= MOE_MAX_PERSLOT_TOKENS) {
         // consecutive launches of up to MOE_MAX_PASS_TOKENS tokens (each validates its part)
         moe_status_t st = check_layer(layer);

@@ -68,4 +68,11 @@ cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, f
                              bool pdl);
 bool expert_tc_supports(int d, int f);
 
+// Host checks shared by the per-slot entry points (api.cu): the status moe_expert_op_perslot
+// returns for these arguments before any device work, leaving out the workspace, and whether
+// a layer runs on the tensor-core path.
+moe_status_t check_perslot_call(const moe_layer_t *L, const void *wg, const void *wu, const void *wd, const void *x,
+                                const int32_t *ids, const float *gates, int32_t n, const float *y);
+bool layer_uses_tc(const moe_layer_t *L);
+
 }  // namespace moe

@@ -25,14 +25,13 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void *g_scratch_addr[kMaxDevices] = {};
-// the (f, m) of the last call's layer on each device: its flag region is in place
-int g_last_shape[kMaxDevices][2] = {};
+// the (f, m) of the tensor-core layer whose flag region was last cleared on each device
+int g_flag_shape[kMaxDevices][2] = {};
 
 // Device address of the scratch on the current device.  In host code the array's name
 // only stands in for it, so the address is looked up once per device, with that device
-// current, and cached.  *shape_changed: the layer's (f, m) differs from the last call's on
-// this device (the tensor-core flags then sit elsewhere and must start from zero).
-cudaError_t scratch_address(const moe_layer_t *layer, void **out, bool *shape_changed) {
+// current, and cached.
+cudaError_t scratch_address(int *dev_out, void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -44,9 +43,7 @@ cudaError_t scratch_address(const moe_layer_t *layer, void **out, bool *shape_ch
         if (e != cudaSuccess) return e;
         g_scratch_addr[dev] = p;
     }
-    *shape_changed = g_last_shape[dev][0] != layer->f || g_last_shape[dev][1] != layer->m;
-    g_last_shape[dev][0] = layer->f;
-    g_last_shape[dev][1] = layer->m;
+    *dev_out = dev;
     *out = g_scratch_addr[dev];
     return cudaSuccess;
 }
@@ -58,21 +55,36 @@ extern "C" moe_status_t moe_expert_op_perslot_noalloc(const moe_layer_t *layer, 
                                                       const int32_t *ids, const float *gates, int32_t n,
                                                       int32_t accumulate, float *y, int32_t *status_out,
                                                       moe_stream_t s) {
-    if (layer == nullptr) return MOE_ERR_ARG;
-    if (moe_workspace_bytes(layer, n) > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
+    // every argument is checked before any device work: a rejected call enqueues nothing
+    const moe_status_t checked = moe::check_perslot_call(layer, w_gate, w_up, w_down, x, ids, gates, n, y);
+    if (checked != MOE_OK) return checked;
     if (status_out != nullptr && (reinterpret_cast<uintptr_t>(status_out) & 3u) != 0) return MOE_ERR_ARG;
+    const size_t need = moe_workspace_bytes(layer, n);
+    if (need > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
+    // the tensor-core path keeps flags after the header; their region, which moe_workspace_bytes
+    // counts, lies inside the scratch by the check above
+    const bool tc = moe::layer_uses_tc(layer);
+    const size_t flag_bytes = tc ? moe::expert_tc_flag_region(layer->f, layer->m) : 0;
+    if (moe::kWorkspaceBytes + flag_bytes > need) return MOE_ERR_WORKSPACE;   // not reachable
+    int dev = 0;
     void *ws = nullptr;
-    bool shape_changed = false;
-    if (scratch_address(layer, &ws, &shape_changed) != cudaSuccess) return MOE_ERR_CUDA;
+    if (scratch_address(&dev, &ws) != cudaSuccess) return MOE_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
     // the previous call's error word must not leak into this one; the epoch word after it
-    // stays.  The flags start from zero when the layer's shape moved them; the partial sums
-    // are written before they are read and need no clearing.
+    // stays.  The flags start from zero when a tensor-core layer of another (f, m) moved
+    // them (partial sums of the old shape may sit where they are now); the partial sums are
+    // written before they are read and need no clearing.
     if (cudaMemsetAsync(ws, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
-    if (shape_changed &&
-        cudaMemsetAsync(static_cast<uint8_t *>(ws) + moe::kWorkspaceBytes, 0,
-                        moe::expert_tc_flag_region(layer->f, layer->m), st) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    if (tc) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (g_flag_shape[dev][0] != layer->f || g_flag_shape[dev][1] != layer->m) {
+            if (cudaMemsetAsync(static_cast<uint8_t *>(ws) + moe::kWorkspaceBytes, 0, flag_bytes, st) != cudaSuccess)
+                return MOE_ERR_CUDA;
+            // recorded only once the clear is enqueued
+            g_flag_shape[dev][0] = layer->f;
+            g_flag_shape[dev][1] = layer->m;
+        }
+    }
     const moe_status_t r = moe_expert_op_perslot(layer, w_gate, w_up, w_down, x, ids, gates, n, accumulate, y, ws,
                                                  kNoAllocScratchBytes, s);
     if (r != MOE_OK) return r;

@@ -92,10 +92,23 @@ def test_noalloc_rejects_layers_beyond_its_scratch(lib):
     P, I32 = ctypes.c_void_p, ctypes.c_int32
     fn.argtypes = [ctypes.POINTER(api.Layer), P, P, P, P, P, P, I32, I32, P, P, P]
     fn.restype = I32
+    # aligned stand-in addresses: every check runs on the host, before any CUDA call (there
+    # is no GPU here, so a call that reached the device would return MOE_ERR_CUDA)
+    fake = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(7)]
     big = api.make_layer(4096, 65536, 128, 64)   # 16 * 64 * 1024 * 1536 bytes of partial sums
     assert lib.moe_workspace_bytes(ctypes.byref(big), 16) > 16 << 20
-    assert fn(ctypes.byref(big), *[None] * 6, 16, 0, None, None, None) == 4   # MOE_ERR_WORKSPACE
-    assert fn(None, *[None] * 6, 1, 0, None, None, None) == 1
+    assert fn(ctypes.byref(big), *fake[:6], 16, 0, fake[6], None, None) == 4   # MOE_ERR_WORKSPACE
+    assert fn(None, *fake[:6], 1, 0, fake[6], None, None) == 1
+    # invalid layers and arguments get the workspace call's statuses, also before any CUDA call
+    assert fn(ctypes.byref(api.make_layer(256, 128, 2, 3)), *fake[:6], 1, 0, fake[6], None, None) == 2   # m > N
+    assert fn(ctypes.byref(api.make_layer(256, 96, 8, 2)), *fake[:6], 1, 0, fake[6], None, None) == 2    # f % 64
+    assert fn(ctypes.byref(api.make_layer(256, 128, 8, 2)), *fake[:6], 65, 0, fake[6], None, None) == 2  # n > 64
+    assert fn(ctypes.byref(api.make_layer(256, 128, 8, 2)), *fake[:6], 0, 0, fake[6], None, None) == 1   # n < 1
+    assert fn(ctypes.byref(api.make_layer(256, 128, 8, 2)), *fake[:3], None, *fake[4:6], 1, 0, fake[6],
+              None, None) == 1   # x missing
+    # a CUDA-core layer needs the header alone, however large its tensor-core flag region would be
+    wide = api.make_layer(64, 65536, 24, 22, "bf16", simt=True)
+    assert lib.moe_workspace_bytes(ctypes.byref(wide), 16) == 256
     mixtral = api.make_layer(4096, 14336, 8, 2)
     assert lib.moe_workspace_bytes(ctypes.byref(mixtral), 16) <= 16 << 20
 
