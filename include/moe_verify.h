@@ -94,14 +94,16 @@ const char *moe_status_str(moe_status_t status);
 /*
  * Bytes of device workspace the expert-operation calls need for this layer and passes
  * of up to n_max tokens: 256 bytes holding the device error word and, for layers the
- * tensor-core kernel runs, a flag region (the per-call release flags with which the kernel's
- * CTAs publish their gate/up shares and their zeroing of y; sized for 16-token passes:
- * round256((1024 + 16*m*(f/64)*12) * 4) bytes) and the fp32 gate/up partial sums the CTAs
- * hand to each other, 3 * 128 * 4 bytes per (slot, 64-row tile of f):
- * 256 + flags + n_max*m*(f/64)*1536 bytes (2.44 MB for d = 2048, f = 768, top-8 at 16 tokens).
- * Zero it once with moe_workspace_init before its first use; calls never clear the flags
- * (each call publishes a new ticket) and rewrite the partial sums before they read them.  A
- * workspace serves layers of one (f, m); zero it again before moving it to another shape.
+ * tensor-core kernel runs, a flag region of 4096 bytes (the per-call flags with which the
+ * kernel's CTAs publish their zeroing of y) and the gate/up partial sums the CTAs hand to
+ * each other, 3 * 128 tagged 64-bit words (an fp32 value and the call's ticket) per (slot,
+ * 64-row tile of f): 256 + 4096 + round256(n_max*m*(f/64)*3072) bytes (4.72 MB for d = 2048,
+ * f = 768, top-8 at 16 tokens).
+ * Zero it once with moe_workspace_init before its first use.  Calls never clear it: every
+ * call takes a new ticket (the workspace counts its calls), and a flag or a partial sum counts
+ * only when it carries the reading call's ticket, so a workspace may move between layers of
+ * any shape without being zeroed again.  Tickets are 32-bit: zero a workspace again at least
+ * once in 2^32 calls.
  * n_max above MOE_MAX_PASS_TOKENS counts as MOE_MAX_PASS_TOKENS.
  */
 size_t moe_workspace_bytes(const moe_layer_t *layer, int32_t n_max);
@@ -216,7 +218,7 @@ moe_status_t moe_expert_op_dedup_ids(const moe_layer_t *layer, const void *w_gat
  *   Arguments and results as moe_expert_op_perslot, without ws/ws_bytes, plus
  *   status_out [dev] int32 [1] or NULL: receives the call's device error word (MOE_OK,
  *   MOE_ERR_BAD_ID or MOE_ERR_DEVICE_TIMEOUT), written on stream s after the kernels.
- * Scratch: a 16 MiB array inside the library, held by every GPU that loads it until the
+ * Scratch: a 32 MiB array inside the library, held by every GPU that loads it until the
  * process exits.  A layer or pass whose workspace (moe_workspace_bytes) would exceed it is
  * rejected with MOE_ERR_WORKSPACE.  Every argument is checked first (the same checks and
  * statuses as moe_expert_op_perslot): a rejected call enqueues no device work.  Its error
@@ -430,6 +432,19 @@ moe_status_t moe_fit_op_times(int32_t count, const int32_t *n, const int32_t *U,
  * infrastructure: no passage of the pages defines it.
  */
 moe_status_t moe_last_device_error(void *ws, moe_stream_t s, int32_t *code);
+
+/*
+ * Sets, for the expert-operation calls issued after it by this process, how many SM clock
+ * cycles one device pipeline wait (a shared-memory barrier, or another CTA's flag) may take
+ * before the call gives up: it then records MOE_ERR_DEVICE_TIMEOUT in the workspace's error
+ * word, waits (bounded) for its copies and tensor-core operations in flight, frees its
+ * tensor memory and returns, leaving the CUDA context usable.  cycles = 0 restores the
+ * default, about two seconds at the maximum clock.  A limit shorter than the call's normal
+ * waits makes it time out: failure detection is tested this way, without a GPU fault.
+ * Library infrastructure: no passage of the pages defines it.  Host only; returns
+ * MOE_ERR_ARG for cycles < 0.
+ */
+moe_status_t moe_set_wait_limit(int64_t cycles);
 
 /*
  * Measurement helper, not part of the method: a read-only streaming probe, the read side of the

@@ -70,7 +70,7 @@ EXPORTED = ("moe_abi_version", "moe_status_str", "moe_workspace_bytes", "moe_wor
             "moe_error_bounds", "moe_kstar_separated", "moe_fit_op_times", "moe_expert_op_perslot_fp8",
             "moe_expert_op_dedup_fp8", "moe_quantize_rows_e4m3", "moe_spec_accept",
             "moe_union_cost_workspace_bytes", "moe_union_cost", "moe_expert_op_dedup_ids",
-            "moe_expert_op_dedup_ids_fp8", "moe_read_probe")
+            "moe_expert_op_dedup_ids_fp8", "moe_read_probe", "moe_set_wait_limit")
 
 _lib = None
 
@@ -106,6 +106,7 @@ def lib():
         "moe_expected_union": ([I32, I32, I32], D),
         "moe_best_draft_length": ([P, I32, D], I32),
         "moe_last_device_error": ([P, P, P], I32),
+        "moe_set_wait_limit": ([ctypes.c_int64], I32),
         "moe_staircase": ([P, I32, P, P, P, P], I32),
         "moe_speedup": ([P, I32, I32, D], D),
         "moe_reuse_threshold": ([I32, D, ctypes.POINTER(ThresholdIn)], D),
@@ -178,6 +179,12 @@ def last_device_error(ws: torch.Tensor) -> int:
     _check(lib().moe_last_device_error(ctypes.c_void_p(ws.data_ptr()), _stream(ws.device),
                                        ctypes.byref(code)), "moe_last_device_error")
     return int(code.value)
+
+
+def set_wait_limit(cycles: int) -> None:
+    """moe_set_wait_limit: SM cycles one device pipeline wait of later expert calls may take
+    before the call records MOE_ERR_DEVICE_TIMEOUT and returns (0: the default; infrastructure)."""
+    _check(lib().moe_set_wait_limit(int(cycles)), "moe_set_wait_limit")
 
 
 # ---------------------------------------------------------------- the hot path

@@ -6,6 +6,7 @@
 // §2 "Testing the inputs"), E[U] under uniform routing (§1) and the best draft length
 // (§1 "Speculative decoding").
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <vector>
@@ -32,6 +33,10 @@ using namespace moe;
 namespace {
 
 constexpr bool kUsePdl = true;
+
+// Cycles a device pipeline wait of the expert kernels may take (0: kWaitLimitCycles); set
+// with moe_set_wait_limit.
+std::atomic<long long> g_wait_limit{0};
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 // ids, gates, logits and groupings are read one element at a time: 4-byte alignment suffices
@@ -97,6 +102,8 @@ ExpertArgs make_args(const moe_layer_t *L, const void *wg, const void *wu, const
     a.mode = mode;
     a.w_dtype = L->w_dtype;
     a.x_dtype = L->x_dtype;
+    const long long wl = g_wait_limit.load(std::memory_order_relaxed);
+    a.wait_limit = wl > 0 ? wl : kWaitLimitCycles;
     return a;
 }
 
@@ -110,7 +117,7 @@ moe_status_t run_expert(const moe_layer_t *L, const ExpertArgs &a, int max_group
         ExpertArgs at = a;
         at.sync = &static_cast<DeviceWorkspace *>(ws)->sync[0];
         at.flags = reinterpret_cast<uint32_t *>(w8 + kWorkspaceBytes);
-        float *part = reinterpret_cast<float *>(w8 + kWorkspaceBytes + expert_tc_flag_region(L->f, L->m));
+        uint64_t *part = reinterpret_cast<uint64_t *>(w8 + kWorkspaceBytes + expert_tc_flag_region(L->f, L->m));
         e = launch_expert_tc(at, max_groups, !accumulate, part, s, kUsePdl);
     } else {
         e = cudaSuccess;
@@ -153,6 +160,12 @@ size_t x_elt_bytes(const moe_layer_t *L) { return L->x_dtype == MOE_BF16 ? 2u : 
 extern "C" {
 
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+moe_status_t moe_set_wait_limit(int64_t cycles) {
+    if (cycles < 0) return MOE_ERR_ARG;
+    g_wait_limit.store(cycles, std::memory_order_relaxed);
+    return MOE_OK;
+}
 
 const char *moe_status_str(moe_status_t status) {
     switch (status) {

@@ -99,16 +99,17 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity.  Gives up when *abort becomes
-// non-zero (another role gave up) or after kWaitLimitCycles; on a time-out it raises the
-// abort flag and records MOE_ERR_DEVICE_TIMEOUT.  Returns true when the phase completed.
+// non-zero (another role gave up) or after `limit` cycles (kWaitLimitCycles unless the call
+// asked for a shorter limit); on a time-out it raises the abort flag and records
+// MOE_ERR_DEVICE_TIMEOUT.  Returns true when the phase completed.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int32_t *abort,
-                                          int32_t *err) {
+                                          int32_t *err, long long limit = kWaitLimitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit) {
             *abort = 1;
             record_error(err, MOE_ERR_DEVICE_TIMEOUT);
             return false;
@@ -119,8 +120,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // Warp-wide forms for warp-uniform code.  Every lane polls and acquires for itself (one
 // polling lane with a broadcast measured slower on GB300), and the outcome is made uniform
 // so that .sync.aligned instructions after it stay converged.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int32_t *abort, int32_t *err) {
-    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort, err));
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int32_t *abort, int32_t *err,
+                                          long long limit = kWaitLimitCycles) {
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort, err, limit));
 }
 // One arrival for the whole warp, after every lane's earlier work (barrier counts are in warps).
 __device__ __forceinline__ void warp_arrive(uint32_t bar) {
@@ -155,12 +157,12 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v
 // have none).  The same abort and time-limit rules as mbar_wait; the outcome is warp-uniform,
 // and every lane's later loads are ordered after the flags it waited for.
 __device__ __forceinline__ bool warp_wait_ticket(const uint32_t *p, uint32_t ticket, volatile int32_t *abort,
-                                                 int32_t *err) {
+                                                 int32_t *err, long long limit = kWaitLimitCycles) {
     bool ok = p == nullptr || ld_acquire_gpu(p) == ticket;
     const long long t0 = clock64();
     while (!__all_sync(0xFFFFFFFFu, ok)) {
         if (!ok) ok = ld_acquire_gpu(p) == ticket;
-        const bool late = clock64() - t0 > kWaitLimitCycles;
+        const bool late = clock64() - t0 > limit;
         if (__any_sync(0xFFFFFFFFu, late || *abort != 0)) {
             if (late) {
                 *abort = 1;

@@ -39,32 +39,34 @@ struct ExpertArgs {
     uint32_t *sync;
     uint32_t *flags;
     int d, f, N, m, n, mode, w_dtype, x_dtype;
+    // cycles a pipeline wait may take before the call gives up with MOE_ERR_DEVICE_TIMEOUT
+    long long wait_limit;
 };
 
 cudaError_t launch_expert_simt(const ExpertArgs &a, int groups, cudaStream_t s, bool pdl);
 
 // Tensor-core path (bf16 or e4m3): one kernel, one CTA per SM.  Its CTAs share each
 // (group, f tile) gate/up item's k blocks, at most kMaxSpan CTAs to an item, and hand their
-// fp32 partial sums to the CTAs that form h through `part`: kMaxSpan * 128 floats per (slot
-// position, f tile), expert_tc_partial_bytes in all, each share published by release flags
-// in `flags` (expert_tc_flag_bytes; zero when the workspace is initialised, never cleared
-// afterwards).  zero_y: y is overwritten (zeroed inside the kernel) rather than added to.
-// Returns cudaErrorNotSupported when the shape is outside what it handles (the caller then
-// reports MOE_ERR_UNSUPPORTED).
+// fp32 partial sums to the CTAs that form h through `part`: kMaxSpan * 128 tagged 64-bit words
+// (value and the call's ticket) per (slot position, f tile), expert_tc_partial_bytes in all.
+// `flags` (expert_tc_flag_bytes) holds the y-zeroing flags of each (CTA, epilogue warp).
+// Neither region needs clearing between calls: everything in them carries a call's ticket,
+// and the workspace is zeroed once when it is initialised.  zero_y: y is overwritten (zeroed
+// inside the kernel) rather than added to.  Returns cudaErrorNotSupported when the shape is
+// outside what it handles (the caller then reports MOE_ERR_UNSUPPORTED).
 constexpr int kMaxSpan = 3;
 constexpr int kMaxGrid = 256;   // CTAs of one call at most
 inline size_t expert_tc_partial_bytes(int f, int m, int n) {
-    return static_cast<size_t>(n) * m * (f / kFTile) * kMaxSpan * 128 * sizeof(float);
+    return static_cast<size_t>(n) * m * (f / kFTile) * kMaxSpan * 128 * sizeof(uint64_t);
 }
 inline size_t expert_tc_flag_bytes(int f, int m, int n) {
-    return (static_cast<size_t>(kMaxGrid) * 4 + static_cast<size_t>(n) * m * (f / kFTile) * kMaxSpan * 4) *
-           sizeof(uint32_t);
+    (void)f, (void)m, (void)n;
+    return static_cast<size_t>(kMaxGrid) * 4 * sizeof(uint32_t);
 }
 inline size_t round256(size_t bytes) { return (bytes + 255) / 256 * 256; }
-// The workspace's flag region: sized for full passes, so that its place and size do not
-// depend on the pass (the partial sums follow it).
+// The workspace's flag region: its size does not depend on the pass (the partial sums follow it).
 inline size_t expert_tc_flag_region(int f, int m) { return round256(expert_tc_flag_bytes(f, m, kMaxPassTokens)); }
-cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, float *part, cudaStream_t s,
+cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, uint64_t *part, cudaStream_t s,
                              bool pdl);
 bool expert_tc_supports(int d, int f);
 

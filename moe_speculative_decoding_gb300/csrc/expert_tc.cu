@@ -111,7 +111,7 @@ struct Elt {
     static constexpr int UNIT = kUnit;
     static constexpr int ITEM = kUnit * TPB;
     static constexpr int COLS = ITEM * 64 / 32;   // f columns of an item per h-former lane
-    static constexpr int TK = F8 ? 2 : 4;         // tokens per round of the h formers' loads
+    static constexpr int TK = F8 ? 1 : 2;         // tokens per round of the h formers' loads (64-bit tagged words)
     __device__ __forceinline__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
         if constexpr (F8) tc_mma_f8(d, a, b, IDESC, acc);
         else tc_mma_bf16(d, a, b, IDESC, acc);
@@ -238,11 +238,22 @@ __device__ __forceinline__ void drain_copies(uint32_t bar_full, uint32_t cnt, in
         mbar_wait_drain(bar_full + 8u * (j % stages), (j / stages) & 1u, kDrainCycles);
 }
 
-// Flag of epilogue warp q for CTA share `slot` of gate/up item `item`; the first
-// kMaxGrid * 4 flags are the y-zeroing flags of (CTA, warp).
-__device__ __forceinline__ uint32_t *gu_flag(uint32_t *flags, int item, int slot, int q) {
-    return flags + kMaxGrid * 4 + (static_cast<size_t>(item) * kMaxSpan + slot) * 4 + q;
+// Tagged partial sums: a value's fp32 bits in the low word and the call's ticket in the high
+// word, stored and loaded as one aligned 64-bit access, which is single-copy atomic.  A reader
+// that finds its call's ticket in a word has the value that was stored with it: the data is its
+// own flag, so no release store and no separate flag sit between a gate/up share and the h
+// formers waiting for it.  Words from earlier calls carry older tickets and never match.
+__device__ __forceinline__ void st_tagged(uint64_t *p, float v, uint32_t ticket) {
+    const uint64_t w = (static_cast<uint64_t>(ticket) << 32) | __float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
+__device__ __forceinline__ uint64_t ld_tagged(const uint64_t *p) {
+    uint64_t w;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+__device__ __forceinline__ bool tag_is(uint64_t w, uint32_t ticket) { return static_cast<uint32_t>(w >> 32) == ticket; }
+__device__ __forceinline__ float tagged_value(uint64_t w) { return __uint_as_float(static_cast<uint32_t>(w)); }
 
 // The call's ticket: the epoch word plus one, never 0 (zeroed flags never match it).
 __device__ __forceinline__ uint32_t call_ticket(const uint32_t *sync) {
@@ -347,7 +358,7 @@ template <bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
                  const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_x,
-                 const ExpertArgs a, float *const part, const int zero_y) {
+                 const ExpertArgs a, uint64_t *const part, const int zero_y) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -370,6 +381,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const long long wl = a.wait_limit;   // cycles before a wait gives up
 
     // ---------------------------------------------------------------- setup
     if (threadIdx.x == 0) {
@@ -486,6 +498,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         return u;
     };
 
+    uint32_t prod_cnt = 0;   // copies the producer issued
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         // The whole warp walks the schedule and waits; one elected lane issues the copies.
@@ -498,7 +511,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             const int row = s.e * a.f + s.tile * kFTile;
             for (long long bb = s.b0; bb < s.b1; ++bb) {
                 const uint32_t st = cnt % kStages, ph = (cnt / kStages) & 1u;
-                if (!warp_wait(bar_empty + 8u * st, ph ^ 1u, abort_flag, a.err)) {
+                if (!warp_wait(bar_empty + 8u * st, ph ^ 1u, abort_flag, a.err, wl)) {
                     ok = false;
                     break;
                 }
@@ -522,7 +535,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             for (int ob = u.ob_first(); ok && ob <= u.ob_last(); ++ob) {
                 for (int sub = u.s_lo(ob); sub < u.s_hi(ob); ++sub) {
                     const uint32_t st = cnt % kStages, ph = (cnt / kStages) & 1u;
-                    if (!warp_wait(bar_empty + 8u * st, ph ^ 1u, abort_flag, a.err)) {
+                    if (!warp_wait(bar_empty + 8u * st, ph ^ 1u, abort_flag, a.err, wl)) {
                         ok = false;
                         break;
                     }
@@ -537,7 +550,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 }
             }
         }
-        if (!ok && lane == 0) drain_copies(bar_full, cnt, kStages);
+        prod_cnt = cnt;
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -550,7 +563,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             if (!s.valid) continue;
             const uint32_t buf = seg % kGuBufs, sph = (seg / kGuBufs) & 1u;
             ++seg;
-            if (!warp_wait(bar_gacc_empty + 8u * buf, sph ^ 1u, abort_flag, a.err)) {
+            if (!warp_wait(bar_gacc_empty + 8u * buf, sph ^ 1u, abort_flag, a.err, wl)) {
                 ok = false;
                 break;
             }
@@ -558,7 +571,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             const uint32_t d_tmem = tmem + 16u * buf;
             for (long long bb = s.b0; bb < s.b1; ++bb) {
                 const uint32_t st = cnt % kStages, ph = (cnt / kStages) & 1u;
-                if (!warp_wait(bar_full + 8u * st, ph, abort_flag, a.err)) {
+                if (!warp_wait(bar_full + 8u * st, ph, abort_flag, a.err, wl)) {
                     ok = false;
                     break;
                 }
@@ -585,7 +598,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             const Units u = units_of(sg);
             const uint32_t hb = run % kHRing, hph = (run / kHRing) & 1u;
             ++run;
-            if (!warp_wait(bar_h_full + 8u * hb, hph, abort_flag, a.err)) {
+            if (!warp_wait(bar_h_full + 8u * hb, hph, abort_flag, a.err, wl)) {
                 ok = false;
                 break;
             }
@@ -596,14 +609,14 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 if (s0 >= s1) continue;
                 const uint32_t buf = dcnt % kDownBufs, dph = (dcnt / kDownBufs) & 1u;
                 ++dcnt;
-                if (!warp_wait(bar_dacc_empty + 8u * buf, dph ^ 1u, abort_flag, a.err)) {
+                if (!warp_wait(bar_dacc_empty + 8u * buf, dph ^ 1u, abort_flag, a.err, wl)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 for (int sub = s0; sub < s1; ++sub) {
                     const uint32_t st = cnt % kStages, ph = (cnt / kStages) & 1u;
-                    if (!warp_wait(bar_full + 8u * st, ph, abort_flag, a.err)) {
+                    if (!warp_wait(bar_full + 8u * st, ph, abort_flag, a.err, wl)) {
                         ok = false;
                         break;
                     }
@@ -678,7 +691,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             const uint32_t buf = seg % kGuBufs, sph = (seg / kGuBufs) & 1u;
             ++seg;
             // wait outcomes are made warp-uniform so the .sync.aligned TMEM loads stay converged
-            if (!warp_wait(bar_gacc_full + 8u * buf, sph, abort_flag, a.err)) {
+            if (!warp_wait(bar_gacc_full + 8u * buf, sph, abort_flag, a.err, wl)) {
                 ok = false;
                 break;
             }
@@ -696,16 +709,14 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             }
 #pragma unroll
             for (int t = 0; t < kNT; ++t)
-                if ((gi.mask >> t) & 1u) part[part_index(gi.pos[t], T, s.tile, slot, row)] = v[t];
-            __syncwarp();
-            if (lane == 0) st_release_gpu(gu_flag(a.flags, s.item, slot, q), ticket);
+                if ((gi.mask >> t) & 1u) st_tagged(part + part_index(gi.pos[t], T, s.tile, slot, row), v[t], ticket);
         }
         // down: y[t, o] += gate_t * (W_down h)[o, t] with the run's gates from its group record
         if (ok && zero_y && dlo < dhi) {
             // every CTA's zeroing of y is visible before the first atomic
             for (int j0 = 0; ok && j0 < 4 * P; j0 += 32) {
                 const int j = j0 + lane;
-                ok = warp_wait_ticket(j < 4 * P ? a.flags + j : nullptr, ticket, abort_flag, a.err);
+                ok = warp_wait_ticket(j < 4 * P ? a.flags + j : nullptr, ticket, abort_flag, a.err, wl);
             }
         }
         uint32_t dcnt = 0, run = 0;
@@ -716,7 +727,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             const Units u = units_of(sg);
             const uint32_t hb = run % kHRing, hph = (run / kHRing) & 1u;
             ++run;
-            if (!warp_wait(bar_h_full + 8u * hb, hph, abort_flag, a.err)) break;
+            if (!warp_wait(bar_h_full + 8u * hb, hph, abort_flag, a.err, wl)) break;
             const uint32_t *const rec = reinterpret_cast<const uint32_t *>(info_ptr + hb * kInfoBytes);
             const uint32_t mask = rec[0];
             float gt[kNT];
@@ -754,7 +765,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                     // already complete (a non-blocking test), so a batch never holds back
                     // finished accumulators
                     if (j > 0 && !__all_sync(kFull, mbar_test_wait(bar_dacc_full + 8u * buf, dph))) break;
-                    if (!warp_wait(bar_dacc_full + 8u * buf, dph, abort_flag, a.err)) {
+                    if (!warp_wait(bar_dacc_full + 8u * buf, dph, abort_flag, a.err, wl)) {
                         ok = false;
                         break;
                     }
@@ -845,21 +856,8 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 span[tl] = min(gsp.part_of(first + KB - 1) - p0[tl] + 1, kMaxSpan);
             }
             // a warp arrives for a run only after its entry is free, so no arrival runs ahead
-            if (!warp_wait(bar_h_empty + 8u * hb, hph ^ 1u, abort_flag, a.err)) break;
-            // the flags of the tiles' shares, 12 per tile (3 shares x 4 epilogue warps): flag
-            // l + 32 r waits in lane l, round r; a warp with no token of the run waits for none
-            bool flags_ok = true;
-#pragma unroll
-            for (int r = 0; r < (E::ITEM * 12 + 31) / 32; ++r) {
-                if (mine == 0) break;
-                const int fi = lane + 32 * r, ftl = fi / 12, fsl = (fi % 12) / 4;
-                const uint32_t *fp = nullptr;
-#pragma unroll
-                for (int tl = 0; tl < E::ITEM; ++tl)
-                    if (ftl == tl && tl < ntiles && fsl < span[tl]) fp = gu_flag(a.flags, sg.g * T + tile0 + tl, fsl, fi & 3);
-                flags_ok = flags_ok && warp_wait_ticket(fp, ticket, abort_flag, a.err);
-            }
-            if (!flags_ok) break;
+            if (!warp_wait(bar_h_empty + 8u * hb, hph ^ 1u, abort_flag, a.err, wl)) break;
+            bool parts_ok = true;
             uint8_t *const hp = h_ptr + hb * kHEntry;
             uint32_t *const rec = reinterpret_cast<uint32_t *>(info_ptr + hb * kInfoBytes);
             // E::TK of this warp's tokens at a time: all loads first (predicated, independent)
@@ -875,22 +873,63 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
 #pragma unroll
                     for (int t = 0; t < kNT; ++t) pk[j] = (tk[j] == static_cast<uint32_t>(t)) ? gi.pos[t] : pk[j];
                 }
-                float pg[E::TK][E::COLS][kMaxSpan], pu[E::TK][E::COLS][kMaxSpan];
+                // the tagged partial sums of these tokens: all loads first (predicated,
+                // independent), then reloads of the words that do not carry this call's ticket
+                // yet, until every word of the warp does (bounded like every wait); words that
+                // are not needed count as present with value 0
+                uint64_t wg[E::TK][E::COLS][kMaxSpan], wu[E::TK][E::COLS][kMaxSpan];
+                const uint64_t absent = static_cast<uint64_t>(ticket) << 32;
 #pragma unroll
                 for (int j = 0; j < E::TK; ++j) {
 #pragma unroll
                     for (int k = 0; k < E::COLS; ++k) {
                         const int c = lane + 32 * k, tl = c >> 6, i = c & 63;
                         const bool on = tk[j] < static_cast<uint32_t>(kNT) && tl < ntiles;
-                        const float *const pp = part + part_index(pk[j], T, tile0 + (on ? tl : 0), 0, i);
+                        const uint64_t *const pp = part + part_index(pk[j], T, tile0 + (on ? tl : 0), 0, i);
 #pragma unroll
                         for (int sl = 0; sl < kMaxSpan; ++sl) {
                             const bool ld = on && sl < span[tl];
-                            pg[j][k][sl] = ld ? __ldcg(pp + sl * 128) : 0.0f;
-                            pu[j][k][sl] = ld ? __ldcg(pp + sl * 128 + 64) : 0.0f;
+                            wg[j][k][sl] = ld ? ld_tagged(pp + sl * 128) : absent;
+                            wu[j][k][sl] = ld ? ld_tagged(pp + sl * 128 + 64) : absent;
                         }
                     }
                 }
+                const long long tp0 = clock64();
+                while (true) {
+                    bool have = true;
+#pragma unroll
+                    for (int j = 0; j < E::TK; ++j)
+#pragma unroll
+                        for (int k = 0; k < E::COLS; ++k)
+#pragma unroll
+                            for (int sl = 0; sl < kMaxSpan; ++sl)
+                                have = have && tag_is(wg[j][k][sl], ticket) && tag_is(wu[j][k][sl], ticket);
+                    if (__all_sync(kFull, have)) break;
+                    const bool late = clock64() - tp0 > wl;
+                    if (__any_sync(kFull, late || *abort_flag != 0)) {
+                        if (late && lane == 0) {
+                            *abort_flag = 1;
+                            record_error(a.err, MOE_ERR_DEVICE_TIMEOUT);
+                        }
+                        parts_ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int j = 0; j < E::TK; ++j) {
+#pragma unroll
+                        for (int k = 0; k < E::COLS; ++k) {
+                            const int c = lane + 32 * k, tl = c >> 6, i = c & 63;
+                            const bool on = tk[j] < static_cast<uint32_t>(kNT) && tl < ntiles;
+                            const uint64_t *const pp = part + part_index(pk[j], T, tile0 + (on ? tl : 0), 0, i);
+#pragma unroll
+                            for (int sl = 0; sl < kMaxSpan; ++sl) {
+                                if (!tag_is(wg[j][k][sl], ticket)) wg[j][k][sl] = ld_tagged(pp + sl * 128);
+                                if (!tag_is(wu[j][k][sl], ticket)) wu[j][k][sl] = ld_tagged(pp + sl * 128 + 64);
+                            }
+                        }
+                    }
+                }
+                if (!parts_ok) break;
 #pragma unroll
                 for (int j = 0; j < E::TK; ++j) {
                     const uint32_t t = tk[j];
@@ -898,7 +937,8 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                     float hv[E::COLS];
 #pragma unroll
                     for (int k = 0; k < E::COLS; ++k)
-                        hv[k] = silu(pg[j][k][0] + pg[j][k][1] + pg[j][k][2]) * (pu[j][k][0] + pu[j][k][1] + pu[j][k][2]);
+                        hv[k] = silu(tagged_value(wg[j][k][0]) + tagged_value(wg[j][k][1]) + tagged_value(wg[j][k][2])) *
+                                (tagged_value(wu[j][k][0]) + tagged_value(wu[j][k][1]) + tagged_value(wu[j][k][2]));
                     if constexpr (!F8) {
 #pragma unroll
                         for (int k = 0; k < E::COLS; ++k) {
@@ -931,6 +971,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                     }
                 }
             }
+            if (!parts_ok) break;
             // the run's record (mask and gates) by the warp of its first token; the epilogue
             // reads the h scales of the mask's tokens only
             if (first == 0 && lane == 0) {
@@ -947,6 +988,10 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
+    // After an abort, copies that no MMA consumed may still be landing: every role has left
+    // its loop (the abort flag is final here), and the CTA waits (bounded) for them to land
+    // before it exits.
+    if (warp == 0 && lane == 0 && *abort_flag != 0) drain_copies(bar_full, prod_cnt, kStages);
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -1005,7 +1050,7 @@ cudaError_t set_attributes() {
 }
 
 template <bool F8>
-cudaError_t launch(const ExpertArgs &a, int sms, int max_groups, bool zero_y, float *part, cudaStream_t s, bool pdl) {
+cudaError_t launch(const ExpertArgs &a, int sms, int max_groups, bool zero_y, uint64_t *part, cudaStream_t s, bool pdl) {
     using E = Elt<F8>;
     const long long T = a.f / kFTile, OBS = a.d / kOB;
     const long long T2 = (T + E::ITEM - 1) / E::ITEM;
@@ -1038,7 +1083,7 @@ cudaError_t launch(const ExpertArgs &a, int sms, int max_groups, bool zero_y, fl
 
 bool expert_tc_supports(int d, int f) { return d % kOB == 0 && f % kFTile == 0 && d >= kOB && f >= kFTile; }
 
-cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, float *part, cudaStream_t s,
+cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, uint64_t *part, cudaStream_t s,
                              bool pdl) {
     const bool f8 = a.w_dtype == MOE_E4M3 && a.x_dtype == MOE_E4M3;
     const bool bf = a.w_dtype == MOE_BF16 && a.x_dtype == MOE_BF16;

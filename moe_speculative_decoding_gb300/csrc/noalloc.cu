@@ -15,23 +15,21 @@ namespace {
 
 // The scratch of moe_expert_op_perslot_noalloc: a workspace (the device error word, then
 // the gate/up partial sums of the tensor-core path) for every layer whose workspace fits
-// 16 MiB, e.g. d = 4096, f = 14336, top-2 at 16 tokens (11 MB).  Every GPU that loads the
+// 32 MiB, e.g. d = 4096, f = 14336, top-2 at 16 tokens (22 MB).  Every GPU that loads the
 // library holds these bytes until the process exits, and every call of the entry point
 // shares them.
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 static_assert(kNoAllocScratchBytes >= moe::kWorkspaceBytes, "scratch smaller than a workspace");
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void *g_scratch_addr[kMaxDevices] = {};
-// the (f, m) of the tensor-core layer whose flag region was last cleared on each device
-int g_flag_shape[kMaxDevices][2] = {};
 
 // Device address of the scratch on the current device.  In host code the array's name
 // only stands in for it, so the address is looked up once per device, with that device
 // current, and cached.
-cudaError_t scratch_address(int *dev_out, void **out) {
+cudaError_t scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -43,7 +41,6 @@ cudaError_t scratch_address(int *dev_out, void **out) {
         if (e != cudaSuccess) return e;
         g_scratch_addr[dev] = p;
     }
-    *dev_out = dev;
     *out = g_scratch_addr[dev];
     return cudaSuccess;
 }
@@ -59,32 +56,15 @@ extern "C" moe_status_t moe_expert_op_perslot_noalloc(const moe_layer_t *layer, 
     const moe_status_t checked = moe::check_perslot_call(layer, w_gate, w_up, w_down, x, ids, gates, n, y);
     if (checked != MOE_OK) return checked;
     if (status_out != nullptr && (reinterpret_cast<uintptr_t>(status_out) & 3u) != 0) return MOE_ERR_ARG;
-    const size_t need = moe_workspace_bytes(layer, n);
-    if (need > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
-    // the tensor-core path keeps flags after the header; their region, which moe_workspace_bytes
-    // counts, lies inside the scratch by the check above
-    const bool tc = moe::layer_uses_tc(layer);
-    const size_t flag_bytes = tc ? moe::expert_tc_flag_region(layer->f, layer->m) : 0;
-    if (moe::kWorkspaceBytes + flag_bytes > need) return MOE_ERR_WORKSPACE;   // not reachable
-    int dev = 0;
+    if (moe_workspace_bytes(layer, n) > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
     void *ws = nullptr;
-    if (scratch_address(&dev, &ws) != cudaSuccess) return MOE_ERR_CUDA;
+    if (scratch_address(&ws) != cudaSuccess) return MOE_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
-    // the previous call's error word must not leak into this one; the epoch word after it
-    // stays.  The flags start from zero when a tensor-core layer of another (f, m) moved
-    // them (partial sums of the old shape may sit where they are now); the partial sums are
-    // written before they are read and need no clearing.
+    // the previous call's error word must not leak into this one.  Everything else in the
+    // scratch carries the ticket of the call that wrote it (the epoch word after the error word
+    // counts the calls), so a later call, of any layer shape, never takes it for its own: it
+    // needs no clearing, and the array starts zeroed when the library loads.
     if (cudaMemsetAsync(ws, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
-    if (tc) {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (g_flag_shape[dev][0] != layer->f || g_flag_shape[dev][1] != layer->m) {
-            if (cudaMemsetAsync(static_cast<uint8_t *>(ws) + moe::kWorkspaceBytes, 0, flag_bytes, st) != cudaSuccess)
-                return MOE_ERR_CUDA;
-            // recorded only once the clear is enqueued
-            g_flag_shape[dev][0] = layer->f;
-            g_flag_shape[dev][1] = layer->m;
-        }
-    }
     const moe_status_t r = moe_expert_op_perslot(layer, w_gate, w_up, w_down, x, ids, gates, n, accumulate, y, ws,
                                                  kNoAllocScratchBytes, s);
     if (r != MOE_OK) return r;

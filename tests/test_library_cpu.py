@@ -66,19 +66,18 @@ def test_argument_validation_before_any_launch(lib):
 
 def test_workspace_bytes(lib):
     """256 header bytes, plus for the tensor-core path its flag region (4 words per CTA for
-    the zeroing of y, 256 CTAs, then 4 epilogue-warp flags per CTA share of a (slot, 64-row f
-    tile) gate/up item, 3 shares, sized for 16-token passes) and 3 CTA shares x 128 fp32
-    partial sums per (slot, 64-row f tile): the gate/up shares' hand-off to the h formers."""
+    the zeroing of y, 256 CTAs) and 3 CTA shares x 128 tagged 64-bit partial sums (value and
+    the call's ticket) per (slot, 64-row f tile): the gate/up shares' hand-off to the h formers."""
     r256 = lambda b: (b + 255) // 256 * 256
     for (d, f, N, m) in [(2048, 768, 128, 8), (2048, 1408, 64, 6), (4096, 14336, 8, 2), (256, 128, 8, 2)]:
         L = api.make_layer(d, f, N, m, "bf16")
-        flags = r256((256 * 4 + 16 * m * (f // 64) * 3 * 4) * 4)
+        flags = r256(256 * 4 * 4)
         for n in (1, 5, 16):
-            part = n * m * (f // 64) * 3 * 128 * 4
+            part = n * m * (f // 64) * 3 * 128 * 8
             assert lib.moe_workspace_bytes(ctypes.byref(L), n) == 256 + flags + r256(part)
         # passes cap at MOE_MAX_PASS_TOKENS
         assert lib.moe_workspace_bytes(ctypes.byref(L), 64) == lib.moe_workspace_bytes(ctypes.byref(L), 16)
-    assert lib.moe_workspace_bytes(ctypes.byref(api.make_layer(2048, 768, 128, 8)), 16) == 256 + 77824 + 2359296
+    assert lib.moe_workspace_bytes(ctypes.byref(api.make_layer(2048, 768, 128, 8)), 16) == 256 + 4096 + 4718592
     # the SIMT kernel and fp32 layers keep only the header
     assert lib.moe_workspace_bytes(ctypes.byref(api.make_layer(256, 512, 8, 2, "f32")), 16) == 256
     assert lib.moe_workspace_bytes(ctypes.byref(api.make_layer(256, 512, 8, 2, "bf16", simt=True)), 16) == 256
@@ -86,7 +85,7 @@ def test_workspace_bytes(lib):
 
 
 def test_noalloc_rejects_layers_beyond_its_scratch(lib):
-    """The 16 MiB library scratch holds 11 MB for d=4096, f=14336, top-2 at 16 tokens; a
+    """The 32 MiB library scratch holds 22 MB for d=4096, f=14336, top-2 at 16 tokens; a
     layer needing more is refused before any device work (no GPU needed for that)."""
     fn = lib.moe_expert_op_perslot_noalloc
     P, I32 = ctypes.c_void_p, ctypes.c_int32
@@ -95,8 +94,8 @@ def test_noalloc_rejects_layers_beyond_its_scratch(lib):
     # aligned stand-in addresses: every check runs on the host, before any CUDA call (there
     # is no GPU here, so a call that reached the device would return MOE_ERR_CUDA)
     fake = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(7)]
-    big = api.make_layer(4096, 65536, 128, 64)   # 16 * 64 * 1024 * 1536 bytes of partial sums
-    assert lib.moe_workspace_bytes(ctypes.byref(big), 16) > 16 << 20
+    big = api.make_layer(4096, 65536, 128, 64)   # 16 * 64 * 1024 * 3072 bytes of partial sums
+    assert lib.moe_workspace_bytes(ctypes.byref(big), 16) > 32 << 20
     assert fn(ctypes.byref(big), *fake[:6], 16, 0, fake[6], None, None) == 4   # MOE_ERR_WORKSPACE
     assert fn(None, *fake[:6], 1, 0, fake[6], None, None) == 1
     # invalid layers and arguments get the workspace call's statuses, also before any CUDA call
@@ -110,7 +109,7 @@ def test_noalloc_rejects_layers_beyond_its_scratch(lib):
     wide = api.make_layer(64, 65536, 24, 22, "bf16", simt=True)
     assert lib.moe_workspace_bytes(ctypes.byref(wide), 16) == 256
     mixtral = api.make_layer(4096, 14336, 8, 2)
-    assert lib.moe_workspace_bytes(ctypes.byref(mixtral), 16) <= 16 << 20
+    assert lib.moe_workspace_bytes(ctypes.byref(mixtral), 16) <= 32 << 20
 
 
 def test_pass_bytes_matches_oracle(lib, oracle_mod):
@@ -310,3 +309,10 @@ def test_verify_side_calls_validate_on_the_host(lib):
     assert lib.moe_union_cost(good, 8, 4, 2, good, 1000, good, good, 0.5, good, good, good, good, good, good,
                               16, None) == 4
     assert lib.moe_union_cost_workspace_bytes(1000) >= 4 * 12
+
+
+def test_wait_limit_setter(lib):
+    """moe_set_wait_limit is host only: negative limits are refused, 0 restores the default."""
+    assert lib.moe_set_wait_limit(ctypes.c_int64(-1)) == 1
+    assert lib.moe_set_wait_limit(ctypes.c_int64(2000)) == 0
+    assert lib.moe_set_wait_limit(ctypes.c_int64(0)) == 0
