@@ -41,6 +41,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Warm L2 (and the address translation) for the 128-byte lines of [p, p + bytes), thread
+// `tid` of `nthreads` taking every nthreads-th line.  A prefetch reads no value: loads that
+// follow it see whatever was written last.
+__device__ __forceinline__ void prefetch_l2_range(const void *p, size_t bytes, int tid, int nthreads) {
+    if (p == nullptr) return;
+    const char *c = static_cast<const char *>(p);
+    for (size_t off = static_cast<size_t>(tid) * 128; off < bytes; off += static_cast<size_t>(nthreads) * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(c + off));
+}
+
 // One lane of the (fully active) warp returns true.  Issuing tensor-core and TMA
 // instructions from an elected lane inside warp-uniform code keeps their operands in
 // uniform registers; a lone divergent lane issuing them is several times slower.

@@ -65,7 +65,9 @@ constexpr int kNT = 16;                       // MMA N (token columns)
 constexpr uint32_t kWBytes = 16384;           // weight bytes of one block
 constexpr uint32_t kXTileBytes = kNT * 128;   // x of one k slice: 16 rows x 128 B
 constexpr uint32_t kSlotBytes = kWBytes + kXTileBytes;   // a ring slot: gate/up block + x, or down block
-constexpr int kStages = 11;                   // ring slots
+// ring slots: 8 keeps enough copies in flight for the full stream (about 130 KB per SM) while
+// every dependent round trip waits behind fewer of them (11 and 6 measured slower)
+constexpr int kStages = 8;
 constexpr int kDownBufs = 8;                  // TMEM ring of down-block accumulators
 constexpr int kEpiBatch = 4;                  // down blocks per epilogue round
 constexpr int kHRing = 4;
@@ -418,6 +420,22 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Before waiting for the preceding grid: warm L2 and the address translation for the small
+    // inputs every CTA reads first (ids, gates, the grouping, x).  Their values are read only
+    // after the wait.
+    {
+        const int S = a.n * a.m, tid = static_cast<int>(threadIdx.x);
+        const size_t xb = static_cast<size_t>(a.n) * a.d * (F8 ? 1 : 2);
+        prefetch_l2_range(a.ids, static_cast<size_t>(S) * 4, tid, kThreads);
+        prefetch_l2_range(a.gates, static_cast<size_t>(S) * 4, tid, kThreads);
+        prefetch_l2_range(a.x, xb, tid, kThreads);
+        if (a.mode == kModeDedup) {   // the grouping's buffer sizes, as the host validated them
+            const int U = S < a.N ? S : a.N;
+            prefetch_l2_range(a.expert_list, static_cast<size_t>(U) * 4, tid, kThreads);
+            prefetch_l2_range(a.offsets, static_cast<size_t>(U + 1) * 4, tid, kThreads);
+            prefetch_l2_range(a.slot_order, static_cast<size_t>(S) * 4, tid, kThreads);
+        }
+    }
     // Every thread waits for the grids this one depends on before reading any input.  The
     // next grid may launch once every CTA of this one has passed this point, so a CTA that
     // waits for another CTA's flag never holds an SM that CTA still needs.
@@ -442,7 +460,21 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     // The routing every role reads: the call's, or, for the deduplicating form from ids, the
     // grouping this CTA builds here (the same in every CTA).
     ExpertArgs ar = a;
-    if (a.mode == kModeDedupIds) {
+    // A one-token pass whose m ids are distinct and in range (as top-m routing gives them) is
+    // its own grouping: each slot is one distinct expert with one token, so the deduplicating
+    // form reads exactly what the per-slot schedule reads and computes the same sums.  Every
+    // warp checks the ids itself (the same data, so the same answer), and no grouping is built.
+    bool own_grouping = false;
+    if (a.mode == kModeDedupIds && a.n == 1 && a.m <= 32) {
+        const bool in = lane < a.m;
+        const int e = in ? a.ids[lane] : -1;
+        const uint32_t active = __ballot_sync(kFull, in);
+        const uint32_t peers = __match_any_sync(kFull, in ? e : -1 - lane);
+        own_grouping = __all_sync(kFull, !in || (e >= 0 && e < a.N && peers == (1u << lane))) && active != 0u;
+    }
+    if (own_grouping) {
+        ar.mode = kModePerSlot;
+    } else if (a.mode == kModeDedupIds) {
         int32_t *const grp = reinterpret_cast<int32_t *>(base_ptr + kGrpOff);
         int32_t *const lst = grp, *const off = grp + kMaxFusedSlots, *const ord = grp + 2 * kMaxFusedSlots + 1;
         int32_t *const gcount = grp + 3 * kMaxFusedSlots + 1, *const scan = gcount + 1;

@@ -36,7 +36,7 @@ def build(force: bool = False) -> str:
         if force or stale:
             os.makedirs(_BUILD, exist_ok=True)
             tmp = _LIB_PATH + f".tmp{os.getpid()}"
-            subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-Wall", "-Wextra",
+            subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-Wall", "-Wextra", "-fopenmp",
                             "-o", tmp, _SRC, "-lm"], check=True)
             os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -88,8 +88,16 @@ def _load():
         lib.oracle_fx_draw.argtypes = [P, I, ctypes.c_float]
         lib.oracle_fx_draw.restype = ctypes.c_int32
         lib.oracle_union_cost.argtypes = [P, I, I, I, P, I, P, P, D, P, P, P, P, P]
+        lib.oracle_set_threads.argtypes = [I]
+        lib.oracle_set_threads(1)   # single-threaded unless a caller asks for more
         _lib = lib
     return _lib
+
+
+def set_threads(n: int) -> int:
+    """Threads of the expert-operation loops (OpenMP over output rows, which never changes a
+    result bit).  Returns the count in force."""
+    return int(_load().oracle_set_threads(int(n)))
 
 
 def _ptr(a: np.ndarray) -> int:

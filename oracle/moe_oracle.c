@@ -44,10 +44,28 @@
  */
 #include <math.h>
 #include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <stdlib.h>
 #include <string.h>
 
 /* ------------------------------------------------------------------ helpers */
+
+/*
+ * Threads of the expert-operation loops (OpenMP over output rows; 1 when built without
+ * OpenMP).  Returns the count now in force.
+ */
+int oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
 
 static double widen(const void *base, int dtype, size_t idx)
 {
@@ -172,6 +190,9 @@ static void swiglu_expert(int d, int f, int wdt, int xdt, const void *wg, const 
     size_t wbase_gu = (size_t)e * (size_t)f * (size_t)d;
     size_t wbase_d = (size_t)e * (size_t)d * (size_t)f;
     size_t xbase = (size_t)t * (size_t)d;
+    /* Output rows are independent and each is summed by one thread in k (or i) order, so
+     * the thread count (oracle_set_threads) never changes a result bit. */
+    #pragma omp parallel for schedule(static)
     for (int i = 0; i < f; ++i) {
         double g = 0.0, u = 0.0;
         for (int k = 0; k < d; ++k) {
@@ -181,6 +202,7 @@ static void swiglu_expert(int d, int f, int wdt, int xdt, const void *wg, const 
         }
         h[i] = g / (1.0 + exp(-g)) * u;
     }
+    #pragma omp parallel for schedule(static)
     for (int o = 0; o < d; ++o) {
         double acc = 0.0;
         for (int i = 0; i < f; ++i) acc += widen(wd, wdt, wbase_d + (size_t)o * f + i) * h[i];

@@ -39,6 +39,29 @@ def test_repeated_and_bad_ids_match_the_two_calls(oracle_mod):
     assert rel_max_err(y1, ref) <= TOL_BF16
 
 
+@pytest.mark.parametrize("row", [[3, 0, 15, 7], [3, 3, 5, 7], [2, 16, 1, 0], [9, -1, 9, 4]])
+def test_one_token_pass_with_and_without_distinct_ids(oracle_mod, row):
+    """A one-token pass with distinct ids needs no grouping (each slot is its own group); a
+    repeated id (gates added, read once) or an id out of range (skipped, MOE_ERR_BAD_ID) takes
+    the grouping path.  Every case matches the two calls and the oracle."""
+    dl = DeviceLayer(256, 256, 16, 4, "bf16", seed=705)
+    x = dl.activations(1, seed=706)
+    ids_np = np.array([row], np.int32)
+    gates = torch.tensor([[0.4, 0.3, 0.2, 0.1]], device="cuda")
+    ids = torch.from_numpy(ids_np).cuda()
+    bad = bool(((ids_np < 0) | (ids_np >= dl.N)).any())
+    grp = api.group_slots(ids, dl.N, ws=dl.ws)
+    y2 = api.expert_op_dedup(dl.layer, dl.w, x, gates, grp, ws=dl.ws).cpu().numpy()
+    assert api.last_device_error(dl.ws) == (5 if bad else 0)
+    y1 = api.expert_op_dedup_ids(dl.layer, dl.w, x, ids, gates, ws=dl.ws).cpu().numpy()
+    assert api.last_device_error(dl.ws) == (5 if bad else 0)
+    assert rel_max_err(y1, y2) <= 1e-4
+    ok = np.where((ids_np >= 0) & (ids_np < dl.N), ids_np, 0)
+    g = np.where((ids_np >= 0) & (ids_np < dl.N), gates.cpu().numpy(), 0.0)
+    ref = oracle_mod.expert_op_perslot(*dl.host(), synth.host_array(x), ok, g)
+    assert rel_max_err(y1, ref) <= TOL_BF16
+
+
 @pytest.mark.parametrize("n", [1, 3, 16])
 def test_qwen3_shape_matches_oracle_and_overwrite(oracle_mod, n):
     """N = 128 experts, m = 8, d = 2048, f = 768 (smaller N for host copies: 32 experts)."""

@@ -53,6 +53,35 @@ def test_route_ties_and_full_softmax(oracle_mod):
     api.route_topm(e, 4)
 
 
+@pytest.mark.parametrize("N,m", [(128, 8), (64, 6)])
+def test_route_near_ties_at_config_size(oracle_mod, N, m):
+    """Normal logits at the configs' expert counts, with the m-th and (m+1)-th largest made
+    equal, one ulp apart either way, or +0/-0, and an exact tie inside the selected set."""
+    rng = np.random.default_rng(1000 + N + m)
+    n = 96
+    z = rng.standard_normal((n, N)).astype(np.float32)
+    for t in range(n):
+        order = np.argsort(-z[t].astype(np.float64), kind="stable")
+        a, b = order[m - 1], order[m]
+        kind = t % 4
+        if kind == 0:
+            z[t, b] = z[t, a]                                      # exact tie at the boundary
+        elif kind == 1:
+            z[t, b] = np.nextafter(z[t, a], np.float32(-np.inf))   # one ulp below
+        elif kind == 2:
+            z[t, b] = np.nextafter(z[t, a], np.float32(np.inf))    # one ulp above: they swap
+        else:
+            z[t, a], z[t, b] = np.float32(0.0), np.float32(-0.0)   # +0 and -0 compare equal
+            z[t, order[m + 1:]] = -np.abs(z[t, order[m + 1:]]) - 1.0
+            z[t, order[:m - 1]] = np.abs(z[t, order[:m - 1]]) + 1.0
+        if m >= 3:
+            z[t, order[1]] = z[t, order[2]]                        # a tie inside the selected set
+    ids, gates = route(z, m)
+    ref_ids, ref_gates = oracle_mod.route_topm(z, m)
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    assert np.allclose(gates.cpu().numpy(), ref_gates, rtol=2e-6, atol=1e-7)
+
+
 def test_route_nan_logits_stay_valid():
     z = np.random.default_rng(102).standard_normal((8, 16)).astype(np.float32)
     z[:, ::2] = np.nan
@@ -218,9 +247,11 @@ def test_accumulate_adds_and_bad_ids_are_skipped(oracle_mod):
     assert rel_max_err(yb, ref) <= TOL_BF16
 
 
-# ------------------------------------------------- the workloads at full size, sampled
+# ------------------------------------------------- the workloads at full size, every token
 
-def _sampled_full_size(oracle_mod, wl, n, rho_index, tokens):
+def _full_size(oracle_mod, wl, n, rho_index):
+    """A full-size layer of the workload, both forms, every token of the pass against the
+    oracle (each token's output from host copies of its own m experts)."""
     dl = DeviceLayer(wl.d, wl.f, wl.N, wl.m, "bf16", seed=synth.seed_for(wl.index, rho_index=rho_index))
     x = dl.activations(n, seed=synth.seed_for(wl.index, rho_index=rho_index, stream=1))
     _, logits = synth.routing_traces(1, n, wl.N, wl.m, wl.rhos[rho_index],
@@ -230,22 +261,22 @@ def _sampled_full_size(oracle_mod, wl, n, rho_index, tokens):
     assert np.array_equal(ids.cpu().numpy(), ref_ids)
     assert int(grp.num_distinct.item()) == oracle_mod.pass_bytes(wl.d, wl.f, wl.N, ref_ids)["U"]
     xh = synth.host_array(x)
-    for t in tokens:
-        experts = ref_ids[t]
-        sub = dl.host_experts(experts)
-        local = np.arange(wl.m, dtype=np.int32)[None, :].repeat(n, axis=0)
-        y_ref = oracle_mod.expert_op_token(*sub, xh, local, ref_gates, t)
+    local = np.arange(wl.m, dtype=np.int32)[None, :].repeat(n, axis=0)
+    refs = {}
+    for t in range(n):
+        y_ref = oracle_mod.expert_op_token(*dl.host_experts(ref_ids[t]), xh, local, ref_gates, t)
+        refs[t] = y_ref
         rms = np.sqrt(np.mean(y_ref ** 2))
         for y in (ys, yd):
-            assert np.max(np.abs(y[t] - y_ref)) <= TOL_BF16 * rms
-    return dl, x, ys, yd
+            assert np.max(np.abs(y[t] - y_ref)) <= TOL_BF16 * rms, t
+    return dl, x, ys, yd, refs
 
 
 @pytest.mark.parametrize("rho_index", [0, 2])
 def test_deepseek_v2_lite_layer_with_shared_experts(oracle_mod, rho_index):
     wl = DSV2_LITE
     n = 8
-    dl, x, ys, yd = _sampled_full_size(oracle_mod, wl, n, rho_index, tokens=(0, 7))
+    dl, x, ys, yd, refs = _full_size(oracle_mod, wl, n, rho_index)
     # two always-on shared experts through the deduplicating call: ids [0, 1], gates 1
     sh = DeviceLayer(wl.d, wl.f_shared, wl.n_shared, wl.n_shared, "bf16",
                      seed=synth.seed_for(wl.index, stream=9))
@@ -255,20 +286,24 @@ def test_deepseek_v2_lite_layer_with_shared_experts(oracle_mod, rho_index):
     y = torch.from_numpy(yd).cuda()
     api.expert_op_dedup(sh.layer, sh.w, x, sgates, sgrp, y=y, accumulate=True, ws=sh.ws)
     y = y.cpu().numpy()
-    y_sh_ref = oracle_mod.expert_op_token(*sh.host(), synth.host_array(x), np.array([[0, 1]] * n, np.int32),
-                                          np.ones((n, 2)), 3)
-    shared_part = y[3] - yd[3]
-    assert np.max(np.abs(shared_part - y_sh_ref)) <= TOL_BF16 * np.sqrt(np.mean(y_sh_ref ** 2))
+    xh = synth.host_array(x)
+    for t in range(n):
+        # the layer's output of token t: routed experts plus both shared experts
+        y_sh = oracle_mod.expert_op_token(*sh.host(), xh, np.array([[0, 1]] * n, np.int32), np.ones((n, 2)), t)
+        full = refs[t] + y_sh
+        assert np.max(np.abs(y[t] - full)) <= TOL_BF16 * np.sqrt(np.mean(full ** 2)), t
+        shared_part = y[t] - yd[t]
+        assert np.max(np.abs(shared_part - y_sh)) <= TOL_BF16 * np.sqrt(np.mean(y_sh ** 2)), t
 
 
 @pytest.mark.parametrize("rho_index", [0, 1])
 def test_qwen3_layer_full_pass(oracle_mod, rho_index):
-    _sampled_full_size(oracle_mod, QWEN3, 16, rho_index, tokens=(0, 9, 15))
+    _full_size(oracle_mod, QWEN3, 16, rho_index)
 
 
 @pytest.mark.parametrize("rho_index", [0, 1])
 def test_mixtral_layer(oracle_mod, rho_index):
-    _sampled_full_size(oracle_mod, MIXTRAL, 8, rho_index, tokens=(0, 5))
+    _full_size(oracle_mod, MIXTRAL, 8, rho_index)
 
 
 @pytest.mark.parametrize("n", [1, 2, 11])
