@@ -43,7 +43,7 @@ sys.path.insert(0, ROOT)
 
 from moe_speculative_decoding_gb300 import api, synth  # noqa: E402
 from moe_speculative_decoding_gb300 import build as mbuild  # noqa: E402
-from moe_speculative_decoding_gb300.configs import BY_NAME, QWEN3_STACK  # noqa: E402
+from moe_speculative_decoding_gb300.configs import BY_NAME, DSV2_LITE, MIXTRAL, QWEN3, QWEN3_STACK  # noqa: E402
 
 METRIC = "MoE verify-pass expert-op µs and achieved HBM TB/s vs pass size n=1..16"
 UNIT = "TB/s"
@@ -72,6 +72,10 @@ def parse():
     p.add_argument("--no-verify-side", action="store_true", help="skip the accept/reject and union-cost leg")
     p.add_argument("--verify-side-only", action="store_true", help="run only the accept/reject and union-cost leg")
     p.add_argument("--verify-reps", type=int, default=20)
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the page-shaped single-layer workloads (DeepSeek-V2-Lite, Qwen3, Mixtral at each reuse)")
+    p.add_argument("--configs-only", default=None,
+                   help="only the configs leg, for the listed workloads (comma-separated names; prints their JSON)")
     return p.parse_args()
 
 
@@ -541,19 +545,20 @@ def kernel_traffic(kernel: str):
 # --------------------------------------------------------------------- our arm
 
 class StackBench:
-    def __init__(self, wl, layers, n_values, windows, device, use_graph=True):
+    def __init__(self, wl, layers, n_values, windows, device, use_graph=True, rho_index=0, weights=None):
         self.wl, self.L, self.n_values, self.windows, self.dev = wl, layers, n_values, windows, device
         self.layer = api.make_layer(wl.d, wl.f, wl.N, wl.m, "bf16")
         self.use_graph = use_graph
+        self.rho = wl.rhos[rho_index]
         t0 = time.time()
-        self.weights = [synth.expert_weights(wl.N, wl.f, wl.d, torch.bfloat16,
-                                             synth.seed_for(wl.index, layer=l), device=device)
-                        for l in range(layers)]
+        self.weights = weights if weights is not None else [
+            synth.expert_weights(wl.N, wl.f, wl.d, torch.bfloat16, synth.seed_for(wl.index, layer=l), device=device)
+            for l in range(layers)]
         torch.cuda.synchronize(device)
         self.t_weights = time.time() - t0
         T = windows * max(n_values)
-        self.sets, logits = synth.routing_traces(layers, T, wl.N, wl.m, wl.rhos[0],
-                                                 seed=synth.seed_for(wl.index, stream=2))
+        self.sets, logits = synth.routing_traces(layers, T, wl.N, wl.m, self.rho,
+                                                 seed=synth.seed_for(wl.index, rho_index=rho_index, stream=2))
         self.ws = api.workspace(self.layer, 16, device)
         self.per_n = {}
         for n in n_values:
@@ -777,6 +782,8 @@ def run_ours(args, world, rank, local):
         line["fp8"] = fp8_leg(b, args, device, per_n)
     if rank == 0 and not args.no_fit:
         line["fits"] = fit_leg(wl, b.weights[0], device, reps=args.fit_reps)
+    if rank == 0 and not args.no_configs:
+        line["configs"] = configs_leg(device)
     if rank == 0:
         line["hbm_read_probe"] = read_probe_leg(device)
     if rank == 0 and not args.no_verify_side:
@@ -785,6 +792,128 @@ def run_ours(args, world, rank, local):
         line["cpu_baseline"] = cpu_baseline(b)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+# layers of each page-shaped workload in the configs leg: enough that the stack's weights
+# exceed L2 (8.9 GB, 9.7 GB and 11.3 GB), so passes run layer after layer without a flush
+CONFIG_LAYERS = {DSV2_LITE.name: 8, QWEN3.name: 8, MIXTRAL.name: 4}
+
+
+def _time_stack(b: StackBench, warmup: int, steps: int, extra=None):
+    """Warm-up and timed steps of a captured stack; per-n seconds of each timed phase (and of
+    `extra(n)`, a callable that runs one more captured phase after the dedup phase)."""
+    for w in range(warmup):
+        b.step(w)
+        if extra is not None:
+            for n in b.n_values:
+                extra(n)
+    torch.cuda.synchronize(b.dev)
+    phases = b.TIMED + (("extra",) if extra is not None else ())
+    acc = {(n, ph): 0.0 for n in b.n_values for ph in phases}
+    for k in range(steps):
+        w = warmup + k
+        for n in b.n_values:
+            ev = {ph: torch.cuda.Event(enable_timing=True) for ph in ("start",) + phases}
+            b.stage(n, w)
+            ev["start"].record()
+            prev = "start"
+            for ph in b.TIMED:
+                b._run(n, ph)
+                ev[ph].record()
+            if extra is not None:
+                extra(n)
+                ev["extra"].record()
+            torch.cuda.synchronize(b.dev)
+            for ph in phases:
+                acc[(n, ph)] += ev[prev].elapsed_time(ev[ph]) * 1e-3
+                prev = ph
+    return acc
+
+
+def configs_leg(device, warmup: int = 2, steps: int = 3, names=None):
+    """The page-shaped single-layer workloads at every reuse value ([Lan] Table 1, §2: per-model
+    effective bandwidths, u_bar(n), r(n) and the crossover): each as a stack of CONFIG_LAYERS
+    layers run layer after layer, like the headline workload.  Per n: microseconds per layer
+    pass of each form, TB/s on requested bytes, u_bar, r, and the crossover n*.  The
+    DeepSeek-V2-Lite block also times its two always-on shared experts (one deduplicating
+    launch per layer on their own weights, ids [0, 1] for every token, gates 1, accumulated),
+    which the pages count outside the expert operation's bytes."""
+    out = {}
+    for wl in (DSV2_LITE, QWEN3, MIXTRAL):
+        if names is not None and wl.name not in names:
+            continue
+        L = CONFIG_LAYERS[wl.name]
+        weights = [synth.expert_weights(wl.N, wl.f, wl.d, torch.bfloat16, synth.seed_for(wl.index, layer=l),
+                                        device=device) for l in range(L)]
+        shared = None
+        if wl.n_shared:
+            sh_layer = api.make_layer(wl.d, wl.f_shared, wl.n_shared, wl.n_shared, "bf16")
+            shared = dict(layer=sh_layer, ws=api.workspace(sh_layer, 16, device),
+                          w=[synth.expert_weights(wl.n_shared, wl.f_shared, wl.d, torch.bfloat16,
+                                                  synth.seed_for(wl.index, layer=l, stream=9), device=device)
+                             for l in range(L)])
+        block = dict(layers=L, d=wl.d, f=wl.f, N=wl.N, m=wl.m, n_values=f"{wl.n_values[0]}..{wl.n_values[-1]}",
+                     timing="CUDA-graph phases of L expert launches, events between phases; weights > L2",
+                     per_rho={})
+        for ri, rho in enumerate(wl.rhos):
+            b = StackBench(wl, L, list(wl.n_values), warmup + steps, device, rho_index=ri, weights=weights)
+            b.capture()
+            extra = None
+            if shared is not None:
+                graphs = {}
+                # every tensor a captured graph reads or writes must outlive the graph: the per-n
+                # grouping, gates and output stay referenced here until the block is done
+                keep = []
+                for n in b.n_values:
+                    st = b.per_n[n]
+                    y_sh = torch.zeros((L, n, wl.d), dtype=torch.float32, device=device)
+                    sids = torch.tensor([[0, 1]] * n, dtype=torch.int32, device=device)
+                    sg = api.group_slots(sids, wl.n_shared)
+                    sgates = torch.ones((n, wl.n_shared), device=device)
+
+                    def run_shared(st=st, sg=sg, sgates=sgates, y_sh=y_sh):
+                        for l in range(L):
+                            api.expert_op_dedup(shared["layer"], shared["w"][l], st["x"], sgates, sg,
+                                                y=y_sh[l], accumulate=True, ws=shared["ws"])
+                    keep.append((sids, sg, sgates, y_sh))
+                    run_shared()
+                    torch.cuda.synchronize(device)
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g):
+                        run_shared()
+                    graphs[n] = g
+                extra = lambda n: graphs[n].replay()
+            acc = _time_stack(b, warmup, steps, extra)
+            steps_w = range(warmup, warmup + steps)
+            nv = b.n_values
+            bs = [sum(b.per_n[n]["bytes_slot"][w] for w in steps_w) for n in nv]
+            bd = [sum(b.per_n[n]["bytes_dedup"][w] for w in steps_w) for n in nv]
+            ts = [acc[(n, "slot")] for n in nv]
+            td = [acc[(n, "dedup")] for n in nv]
+            rep = api.bandwidth_report(nv[0], bs, bd, ts, td)
+            per_n = []
+            for i, n in enumerate(nv):
+                row = dict(n=n, us_slot=round(ts[i] / (steps * L) * 1e6, 2), us_dedup=round(td[i] / (steps * L) * 1e6, 2),
+                           tbps_slot=round(rep["beta_slot"][i] / 1e12, 3), tbps_dedup=round(rep["beta_dedup"][i] / 1e12, 3),
+                           ubar=round(float(rep["ubar"][i]), 4), r=round(float(rep["r"][i]), 4))
+                if shared is not None:
+                    t_sh = acc[(n, "extra")] / (steps * L)
+                    row["us_shared"] = round(t_sh * 1e6, 2)
+                    row["tbps_shared"] = round(wl.n_shared * 3 * wl.d * wl.f_shared * 2 / t_sh / 1e12, 3)
+                per_n.append(row)
+            assert api.last_device_error(b.ws) == 0
+            block["per_rho"][str(rho)] = dict(per_n=per_n, crossover=rep["crossover"],
+                                             max_slot_vs_dedup_rel=round(b.check_outputs(), 6))
+            torch.cuda.synchronize(device)
+            if shared is not None:
+                assert api.last_device_error(shared["ws"]) == 0
+                del graphs, keep, extra
+            del b
+            torch.cuda.empty_cache()
+        out[wl.name] = block
+        del weights, shared
+        torch.cuda.empty_cache()
+    return out
 
 
 def e2e_run(b: StackBench, args, world, device, total_bytes_per_step):
@@ -924,6 +1053,11 @@ def main():
         # the oracle needs no collective: rank 0 runs it, other ranks exit without work
         world = int(os.environ.get("WORLD_SIZE", "1"))
         run_reference(args, world, int(os.environ.get("RANK", "0")))
+        return
+    if args.configs_only:
+        mbuild.build()
+        device = torch.device("cuda", 0)
+        print(json.dumps(dict(configs=configs_leg(device, names=args.configs_only.split(",")))), flush=True)
         return
     if args.fit_only:
         mbuild.build()

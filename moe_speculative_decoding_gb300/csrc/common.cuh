@@ -156,6 +156,15 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
     return v;
 }
 
+// Relaxed gpu-scope load (several may be in flight at once); followed by fence_acq_rel_gpu once
+// a value written with st_release_gpu was seen, it orders later accesses after that store.
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // gpu-scope atomic add with acquire and release semantics; returns the old value.
 __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v) {
     uint32_t old;
@@ -181,6 +190,41 @@ __device__ __forceinline__ bool warp_wait_ticket(const uint32_t *p, uint32_t tic
             return false;
         }
     }
+    __syncwarp();
+    return true;
+}
+
+// Warp-wide bounded wait until every flag of flags[0, count) holds `ticket` (count <= 32 * 32):
+// lane l watches flags l + 32 r, all of its loads in flight together, so the wait costs one
+// round trip to memory when the flags are already set, not one per 32 flags.  The same abort
+// and time-limit rules as mbar_wait; every lane's later accesses are ordered after the flags.
+__device__ __forceinline__ bool warp_wait_tickets(const uint32_t *flags, int count, uint32_t ticket,
+                                                  volatile int32_t *abort, int32_t *err,
+                                                  long long limit = kWaitLimitCycles) {
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    uint32_t missing = 0;   // bit r: flag lane + 32 r not seen yet
+    for (int r = 0; r < 32; ++r)
+        if (lane + 32 * r < count) missing |= 1u << r;
+    const long long t0 = clock64();
+    while (true) {
+        uint32_t v[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+            if ((missing >> r) & 1u) v[r] = ld_relaxed_gpu(flags + lane + 32 * r);   // all in flight together
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+            if (((missing >> r) & 1u) && v[r] == ticket) missing &= ~(1u << r);
+        if (__all_sync(0xFFFFFFFFu, missing == 0u)) break;
+        const bool late = clock64() - t0 > limit;
+        if (__any_sync(0xFFFFFFFFu, late || *abort != 0)) {
+            if (late) {
+                *abort = 1;
+                record_error(err, MOE_ERR_DEVICE_TIMEOUT);
+            }
+            return false;
+        }
+    }
+    fence_acq_rel_gpu();   // the flags seen (relaxed) now order this lane's later accesses
     __syncwarp();
     return true;
 }

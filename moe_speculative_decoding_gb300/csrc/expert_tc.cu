@@ -745,11 +745,8 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         }
         // down: y[t, o] += gate_t * (W_down h)[o, t] with the run's gates from its group record
         if (ok && zero_y && dlo < dhi) {
-            // every CTA's zeroing of y is visible before the first atomic
-            for (int j0 = 0; ok && j0 < 4 * P; j0 += 32) {
-                const int j = j0 + lane;
-                ok = warp_wait_ticket(j < 4 * P ? a.flags + j : nullptr, ticket, abort_flag, a.err, wl);
-            }
+            // every CTA's zeroing of y is visible before the first atomic (4 P <= 1024 flags)
+            ok = warp_wait_tickets(a.flags, 4 * P, ticket, abort_flag, a.err, wl);
         }
         uint32_t dcnt = 0, run = 0;
         for (long long b = dlo; ok && b < dhi;) {
