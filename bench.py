@@ -74,6 +74,9 @@ def parse():
     p.add_argument("--verify-reps", type=int, default=20)
     p.add_argument("--no-configs", action="store_true",
                    help="skip the page-shaped single-layer workloads (DeepSeek-V2-Lite, Qwen3, Mixtral at each reuse)")
+    p.add_argument("--no-long", action="store_true", help="skip the passes of 17..64 tokens")
+    p.add_argument("--long-only", action="store_true",
+                   help="only the passes of 17..64 tokens on 8 freshly generated layers (prints their JSON)")
     p.add_argument("--configs-only", default=None,
                    help="only the configs leg, for the listed workloads (comma-separated names; prints their JSON)")
     return p.parse_args()
@@ -559,7 +562,7 @@ class StackBench:
         T = windows * max(n_values)
         self.sets, logits = synth.routing_traces(layers, T, wl.N, wl.m, self.rho,
                                                  seed=synth.seed_for(wl.index, rho_index=rho_index, stream=2))
-        self.ws = api.workspace(self.layer, 16, device)
+        self.ws = api.workspace(self.layer, max(16, max(n_values)), device)
         self.per_n = {}
         for n in n_values:
             lw = np.stack([logits[:, w * n:(w + 1) * n, :].reshape(layers * n, wl.N) for w in range(windows)])
@@ -784,6 +787,8 @@ def run_ours(args, world, rank, local):
         line["fits"] = fit_leg(wl, b.weights[0], device, reps=args.fit_reps)
     if rank == 0 and not args.no_configs:
         line["configs"] = configs_leg(device)
+    if rank == 0 and not args.no_long:
+        line["long_pass"] = long_pass_leg(wl, b.weights[:8], device)
     if rank == 0:
         line["hbm_read_probe"] = read_probe_leg(device)
     if rank == 0 and not args.no_verify_side:
@@ -913,6 +918,39 @@ def configs_leg(device, warmup: int = 2, steps: int = 3, names=None):
         out[wl.name] = block
         del weights, shared
         torch.cuda.empty_cache()
+    return out
+
+
+LONG_PASS_N = (17, 24, 32, 40, 48, 64)
+
+
+def long_pass_leg(wl, weights, device, warmup: int = 2, steps: int = 3):
+    """Passes of 17 to 64 tokens on the headline layer shape ([Lan] §1: the deduplicating form
+    reads each distinct expert once per pass; §2: effective bandwidth on requested bytes).  A
+    stack of len(weights) layers run layer after layer (weights > L2), the per-slot calls as
+    launches of up to 16 tokens, the deduplicating call in one launch of the 64-token
+    instantiation (above 256 slots after its in-workspace grouping launch).  Per n:
+    microseconds per layer pass of each form, TB/s on requested bytes, u_bar and r."""
+    L = len(weights)
+    b = StackBench(wl, L, list(LONG_PASS_N), warmup + steps, device, weights=weights)
+    b.capture()
+    acc = _time_stack(b, warmup, steps)
+    steps_w = range(warmup, warmup + steps)
+    nv = b.n_values
+    bs = [sum(b.per_n[n]["bytes_slot"][w] for w in steps_w) for n in nv]
+    bd = [sum(b.per_n[n]["bytes_dedup"][w] for w in steps_w) for n in nv]
+    ts = [acc[(n, "slot")] for n in nv]
+    td = [acc[(n, "dedup")] for n in nv]
+    rep = api.bandwidth_report(nv[0], bs, bd, ts, td)
+    per_n = [dict(n=n, us_slot=round(ts[i] / (steps * L) * 1e6, 2), us_dedup=round(td[i] / (steps * L) * 1e6, 2),
+                  tbps_slot=round(rep["beta_slot"][i] / 1e12, 3), tbps_dedup=round(rep["beta_dedup"][i] / 1e12, 3),
+                  ubar=round(float(rep["ubar"][i]), 4), r=round(float(rep["r"][i]), 4))
+             for i, n in enumerate(nv)]
+    out = dict(layers=L, d=wl.d, f=wl.f, N=wl.N, m=wl.m, rho=b.rho, per_n=per_n,
+               max_slot_vs_dedup_rel=round(b.check_outputs(), 6), device_error=api.last_device_error(b.ws),
+               timing="CUDA-graph phases of L expert launches, events between phases; weights > L2")
+    del b
+    torch.cuda.empty_cache()
     return out
 
 
@@ -1067,6 +1105,14 @@ def main():
         mbuild.build()
         device = torch.device("cuda", 0)
         print(json.dumps(dict(configs=configs_leg(device, names=args.configs_only.split(",")))), flush=True)
+        return
+    if args.long_only:
+        mbuild.build()
+        wl = BY_NAME[args.workload]
+        device = torch.device("cuda", 0)
+        w = [synth.expert_weights(wl.N, wl.f, wl.d, torch.bfloat16, synth.seed_for(wl.index, layer=l), device=device)
+             for l in range(8)]
+        print(json.dumps(dict(workload=wl.name, long_pass=long_pass_leg(wl, w, device))), flush=True)
         return
     if args.fit_only:
         mbuild.build()

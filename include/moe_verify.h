@@ -42,7 +42,7 @@ extern "C" {
 struct CUstream_st;
 typedef struct CUstream_st *moe_stream_t;
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 typedef enum {
     MOE_OK = 0,
@@ -79,9 +79,15 @@ typedef struct {
  * tensor-core kernel is the default for bf16; fp32 layers always use the CUDA cores). */
 #define MOE_FLAG_SIMT 1
 
-/* Largest pass size (tokens per verification pass) the expert operation accepts. */
-#define MOE_MAX_PASS_TOKENS 16
-/* The per-slot calls take passes of up to 64 tokens, as consecutive launches of up to 16. */
+/* Largest pass size (tokens per verification pass) every expert-operation call accepts. */
+#define MOE_MAX_PASS_TOKENS 64
+/* The per-slot calls run a pass above this many tokens as consecutive launches of up to this
+ * many (the per-slot form reads every slot's expert either way), so their workspace needs
+ * only moe_workspace_bytes(layer, MOE_PERSLOT_LAUNCH_TOKENS).  The deduplicating calls run a
+ * pass of up to MOE_MAX_PASS_TOKENS in one launch: a distinct expert is read once for all of
+ * its tokens. */
+#define MOE_PERSLOT_LAUNCH_TOKENS 16
+/* The per-slot calls' pass limit (the same as every call's). */
 #define MOE_MAX_PERSLOT_TOKENS 64
 
 /* Returns MOE_ABI_VERSION.  Library infrastructure: no passage of the pages defines it. */
@@ -104,7 +110,9 @@ const char *moe_status_str(moe_status_t status);
  * only when it carries the reading call's ticket, so a workspace may move between layers of
  * any shape without being zeroed again.  Tickets are 32-bit: zero a workspace again at least
  * once in 2^32 calls.
- * n_max above MOE_MAX_PASS_TOKENS counts as MOE_MAX_PASS_TOKENS.
+ * n_max above MOE_MAX_PASS_TOKENS counts as MOE_MAX_PASS_TOKENS.  For a pass of more than
+ * 256 slots (n_max*m > 256) the deduplicating call from ids also keeps the pass's grouping
+ * there: round256(4 * (2*N + n_max*m + 2)) bytes more.
  */
 size_t moe_workspace_bytes(const moe_layer_t *layer, int32_t n_max);
 
@@ -161,10 +169,10 @@ moe_status_t moe_group_slots(const int32_t *ids, int32_t n, int32_t m, int32_t N
  *   ids   [dev] int32 [n, m];  gates [dev] fp32 [n, m].
  *   y     [dev] fp32 [n, d]    accumulate == 0: y is overwritten; != 0: added to.
  *   ws    [dev] workspace of ws_bytes >= moe_workspace_bytes(layer, n).
- * Supported: 1 <= n <= MOE_MAX_PERSLOT_TOKENS.  A pass above MOE_MAX_PASS_TOKENS runs as
- * consecutive launches of up to MOE_MAX_PASS_TOKENS tokens on s (the per-slot form reads
+ * Supported: 1 <= n <= MOE_MAX_PASS_TOKENS.  A pass above MOE_PERSLOT_LAUNCH_TOKENS runs as
+ * consecutive launches of up to MOE_PERSLOT_LAUNCH_TOKENS tokens on s (the per-slot form reads
  * every slot's expert either way; the launches write disjoint rows of y and share ws, which
- * needs only moe_workspace_bytes(layer, MOE_MAX_PASS_TOKENS)).  Each launch is validated
+ * needs only moe_workspace_bytes(layer, MOE_PERSLOT_LAUNCH_TOKENS)).  Each launch is validated
  * before it is enqueued and the first error ends the call; the chunks share the layer and
  * the pointers' alignment, so an argument error is found before the first launch.
  * Summation order inside y is not fixed (results may differ in the last bits between runs).
@@ -200,8 +208,11 @@ moe_status_t moe_expert_op_dedup(const moe_layer_t *layer, const void *w_gate, c
  * inside the kernel, once per CTA in shared memory, instead of by a launch of its own.
  *   Arguments as moe_expert_op_perslot (ids [dev] int32 [n*m] as there).  Ids outside
  *   [0, N) are left out of every group and set MOE_ERR_BAD_ID in the workspace.
- * Supported: the layers the tensor-core kernel runs (bf16, d a multiple of 128), n*m <= 256;
- * otherwise MOE_ERR_UNSUPPORTED (use the two calls).
+ * A pass of more than 256 slots (n*m > 256, e.g. top-8 above 32 tokens) has its grouping built
+ * by moe_group_slots into the workspace first (two launches, the same result; the workspace
+ * then holds it, see moe_workspace_bytes).
+ * Supported: the layers the tensor-core kernel runs (bf16, d a multiple of 128), 1 <= n <=
+ * MOE_MAX_PASS_TOKENS; otherwise MOE_ERR_UNSUPPORTED.
  */
 moe_status_t moe_expert_op_dedup_ids(const moe_layer_t *layer, const void *w_gate, const void *w_up,
                                      const void *w_down, const void *x, const int32_t *ids, const float *gates,

@@ -18,8 +18,9 @@ from . import build as _build
 
 MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
 MOE_FLAG_SIMT = 1
-MAX_PASS_TOKENS = 16        # tokens per launch of the expert kernel
-MAX_PERSLOT_TOKENS = 64     # tokens per per-slot call (consecutive launches of up to 16)
+MAX_PASS_TOKENS = 64        # tokens per pass of every expert-operation call
+PERSLOT_LAUNCH_TOKENS = 16  # tokens per launch of the per-slot calls (a longer pass is split)
+MAX_PERSLOT_TOKENS = 64     # tokens per per-slot call
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_BAD_ID", 6: "MOE_ERR_DEVICE_TIMEOUT"}
 
@@ -164,8 +165,11 @@ def make_layer(d: int, f: int, N: int, m: int, dtype: str = "bf16", simt: bool =
     return Layer(d, f, N, m, code, code, MOE_FLAG_SIMT if simt else 0)
 
 
-def workspace(layer: Layer, n_max: int = MAX_PASS_TOKENS, device=None) -> torch.Tensor:
-    """A zeroed device workspace for passes of up to n_max tokens (moe_workspace_bytes, moe_workspace_init; infrastructure)."""
+def workspace(layer: Layer, n_max: int = PERSLOT_LAUNCH_TOKENS, device=None) -> torch.Tensor:
+    """A zeroed device workspace for passes of up to n_max tokens (moe_workspace_bytes, moe_workspace_init; infrastructure).
+
+    The default serves per-slot calls of any size (they launch 16 tokens at a time); a
+    deduplicating call of n > 16 tokens needs n_max >= n."""
     nbytes = int(lib().moe_workspace_bytes(ctypes.byref(layer), n_max))
     ws = torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
     _check(lib().moe_workspace_init(ctypes.c_void_p(ws.data_ptr()), nbytes, _stream(ws.device)),

@@ -129,6 +129,33 @@ moe_status_t run_expert(const moe_layer_t *L, const ExpertArgs &a, int max_group
     return cuda_status(e);
 }
 
+// The deduplicating form from ids: the grouping built inside the kernel for up to
+// kMaxFusedSlots slots, else by moe_group_slots' kernel into the workspace (after the partial
+// sums of this pass), followed by the deduplicating kernel on it.
+moe_status_t run_dedup_ids(const moe_layer_t *L, ExpertArgs a, int32_t n, int32_t accumulate, void *ws,
+                           cudaStream_t s) {
+    const int S = n * L->m;
+    const int cap = S < L->N ? S : L->N;
+    if (S <= kMaxFusedSlots) {
+        a.mode = kModeDedupIds;
+        return run_expert(L, a, cap, accumulate, ws, s);
+    }
+    uint8_t *const w8 = static_cast<uint8_t *>(ws);
+    int32_t *const grp = reinterpret_cast<int32_t *>(w8 + kWorkspaceBytes + expert_tc_flag_region(L->f, L->m) +
+                                                     round256(expert_tc_partial_bytes(L->f, L->m, n)));
+    int32_t *const count = grp, *const list = grp + 1, *const offsets = list + L->N, *const order = offsets + L->N + 1;
+    cudaError_t e = launch_group_slots(a.ids, S, L->N, count, list, offsets, order,
+                                       &static_cast<DeviceWorkspace *>(ws)->error, s, kUsePdl);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_status(e);
+    a.mode = kModeDedup;
+    a.num_distinct = count;
+    a.expert_list = list;
+    a.offsets = offsets;
+    a.slot_order = order;
+    return run_expert(L, a, cap, accumulate, ws, s);
+}
+
 }  // namespace
 
 namespace moe {
@@ -139,7 +166,7 @@ moe_status_t check_perslot_call(const moe_layer_t *L, const void *wg, const void
     const moe_status_t st = check_layer(L);
     if (st != MOE_OK) return st;
     if (n < 1) return MOE_ERR_ARG;
-    if (n > MOE_MAX_PERSLOT_TOKENS) return MOE_ERR_UNSUPPORTED;
+    if (n > MOE_MAX_PASS_TOKENS) return MOE_ERR_UNSUPPORTED;
     const void *ptrs[] = {wg, wu, wd, x, y};
     for (const void *p : ptrs)
         if (p == nullptr || !aligned16(p)) return MOE_ERR_ARG;
@@ -183,7 +210,10 @@ const char *moe_status_str(moe_status_t status) {
 size_t moe_workspace_bytes(const moe_layer_t *layer, int32_t n_max) {
     if (check_layer(layer) != MOE_OK || n_max < 1 || !uses_tc(layer)) return kWorkspaceBytes;
     const int n = n_max < MOE_MAX_PASS_TOKENS ? n_max : MOE_MAX_PASS_TOKENS;
-    return kWorkspaceBytes + expert_tc_flag_region(layer->f, layer->m) + round256(expert_tc_partial_bytes(layer->f, layer->m, n));
+    size_t bytes = kWorkspaceBytes + expert_tc_flag_region(layer->f, layer->m) +
+                   round256(expert_tc_partial_bytes(layer->f, layer->m, n));
+    if (n * layer->m > kMaxFusedSlots) bytes += dedup_grouping_bytes(layer->N, n * layer->m);
+    return bytes;
 }
 
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t s) {
@@ -226,14 +256,14 @@ moe_status_t moe_expert_op_perslot(const moe_layer_t *layer, const void *w_gate,
                                    moe_stream_t s) {
     moe_status_t st0 = check_perslot_call(layer, w_gate, w_up, w_down, x, ids, gates, n, y);
     if (st0 != MOE_OK) return st0;
-    if (n > MOE_MAX_PASS_TOKENS && n <= MOE_MAX_PERSLOT_TOKENS) {
-        // consecutive launches of up to MOE_MAX_PASS_TOKENS tokens (each validates its part)
+    if (n > MOE_PERSLOT_LAUNCH_TOKENS && n <= MOE_MAX_PASS_TOKENS) {
+        // consecutive launches of up to MOE_PERSLOT_LAUNCH_TOKENS tokens (each validates its part)
         moe_status_t st = check_layer(layer);
         if (st != MOE_OK) return st;
         if (x == nullptr || ids == nullptr || gates == nullptr || y == nullptr) return MOE_ERR_ARG;
         const size_t xrow = static_cast<size_t>(layer->d) * x_elt_bytes(layer);
-        for (int32_t t0 = 0; t0 < n; t0 += MOE_MAX_PASS_TOKENS) {
-            const int32_t nc = n - t0 < MOE_MAX_PASS_TOKENS ? n - t0 : MOE_MAX_PASS_TOKENS;
+        for (int32_t t0 = 0; t0 < n; t0 += MOE_PERSLOT_LAUNCH_TOKENS) {
+            const int32_t nc = n - t0 < MOE_PERSLOT_LAUNCH_TOKENS ? n - t0 : MOE_PERSLOT_LAUNCH_TOKENS;
             const size_t so = static_cast<size_t>(t0) * layer->m;
             st = moe_expert_op_perslot(layer, w_gate, w_up, w_down, static_cast<const uint8_t *>(x) + t0 * xrow,
                                        ids + so, gates + so, nc, accumulate, y + static_cast<size_t>(t0) * layer->d,
@@ -277,12 +307,11 @@ moe_status_t moe_expert_op_dedup_ids(const moe_layer_t *layer, const void *w_gat
                                      moe_stream_t s) {
     moe_status_t st = check_expert_common(layer, w_gate, w_up, w_down, x, gates, n, y, ws, ws_bytes);
     if (st != MOE_OK) return st;
-    if (is_fp8(layer) || !uses_tc(layer) || n * layer->m > kMaxFusedSlots) return MOE_ERR_UNSUPPORTED;
+    if (is_fp8(layer) || !uses_tc(layer)) return MOE_ERR_UNSUPPORTED;
     if (ids == nullptr || !aligned4(ids)) return MOE_ERR_ARG;
     ExpertArgs a = make_args(layer, w_gate, w_up, w_down, x, gates, n, y, ws, kModeDedupIds);
     a.ids = ids;
-    const int cap = n * layer->m < layer->N ? n * layer->m : layer->N;
-    return run_expert(layer, a, cap, accumulate, ws, reinterpret_cast<cudaStream_t>(s));
+    return run_dedup_ids(layer, a, n, accumulate, ws, reinterpret_cast<cudaStream_t>(s));
 }
 
 namespace {
@@ -297,14 +326,14 @@ moe_status_t moe_expert_op_perslot_fp8(const moe_layer_t *layer, const void *w_g
                                        const void *w_down, const moe_weight_scales_t *scales, const void *x,
                                        const float *x_scale, const int32_t *ids, const float *gates, int32_t n,
                                        int32_t accumulate, float *y, void *ws, size_t ws_bytes, moe_stream_t s) {
-    if (n > MOE_MAX_PASS_TOKENS && n <= MOE_MAX_PERSLOT_TOKENS) {
-        // consecutive launches of up to MOE_MAX_PASS_TOKENS tokens (each validates its part)
+    if (n > MOE_PERSLOT_LAUNCH_TOKENS && n <= MOE_MAX_PASS_TOKENS) {
+        // consecutive launches of up to MOE_PERSLOT_LAUNCH_TOKENS tokens (each validates its part)
         moe_status_t st = check_layer(layer);
         if (st != MOE_OK) return st;
         if (x == nullptr || x_scale == nullptr || ids == nullptr || gates == nullptr || y == nullptr) return MOE_ERR_ARG;
         const size_t xrow = static_cast<size_t>(layer->d) * x_elt_bytes(layer);
-        for (int32_t t0 = 0; t0 < n; t0 += MOE_MAX_PASS_TOKENS) {
-            const int32_t nc = n - t0 < MOE_MAX_PASS_TOKENS ? n - t0 : MOE_MAX_PASS_TOKENS;
+        for (int32_t t0 = 0; t0 < n; t0 += MOE_PERSLOT_LAUNCH_TOKENS) {
+            const int32_t nc = n - t0 < MOE_PERSLOT_LAUNCH_TOKENS ? n - t0 : MOE_PERSLOT_LAUNCH_TOKENS;
             const size_t so = static_cast<size_t>(t0) * layer->m;
             st = moe_expert_op_perslot_fp8(layer, w_gate, w_up, w_down, scales,
                                            static_cast<const uint8_t *>(x) + t0 * xrow, x_scale + t0, ids + so,
@@ -333,7 +362,7 @@ moe_status_t moe_expert_op_dedup_ids_fp8(const moe_layer_t *layer, const void *w
                                          int32_t accumulate, float *y, void *ws, size_t ws_bytes, moe_stream_t s) {
     moe_status_t st = check_expert_common(layer, w_gate, w_up, w_down, x, gates, n, y, ws, ws_bytes);
     if (st != MOE_OK) return st;
-    if (!is_fp8(layer) || n * layer->m > kMaxFusedSlots) return MOE_ERR_UNSUPPORTED;
+    if (!is_fp8(layer)) return MOE_ERR_UNSUPPORTED;
     if (ids == nullptr || !aligned4(ids) || !fp8_scales_ok(scales, x_scale)) return MOE_ERR_ARG;
     ExpertArgs a = make_args(layer, w_gate, w_up, w_down, x, gates, n, y, ws, kModeDedupIds);
     a.ids = ids;
@@ -341,8 +370,7 @@ moe_status_t moe_expert_op_dedup_ids_fp8(const moe_layer_t *layer, const void *w
     a.s_up = scales->up;
     a.s_down = scales->down;
     a.s_x = x_scale;
-    const int cap = n * layer->m < layer->N ? n * layer->m : layer->N;
-    return run_expert(layer, a, cap, accumulate, ws, reinterpret_cast<cudaStream_t>(s));
+    return run_dedup_ids(layer, a, n, accumulate, ws, reinterpret_cast<cudaStream_t>(s));
 }
 
 moe_status_t moe_expert_op_dedup_fp8(const moe_layer_t *layer, const void *w_gate, const void *w_up,

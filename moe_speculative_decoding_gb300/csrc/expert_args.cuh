@@ -7,7 +7,8 @@
 
 namespace moe {
 
-constexpr int kMaxPassTokens = MOE_MAX_PASS_TOKENS;   // tokens per pass (MMA N = 16)
+constexpr int kMaxPassTokens = MOE_MAX_PASS_TOKENS;   // tokens per pass (MMA N = 16, or 64 above 16)
+constexpr int kPerSlotLaunchTokens = MOE_PERSLOT_LAUNCH_TOKENS;   // tokens per launch of the per-slot calls
 constexpr int kFTile = 64;                             // rows of f per work item
 
 // kModeDedupIds: the deduplicating form from the slots' ids, the grouping built inside the
@@ -64,6 +65,9 @@ inline size_t expert_tc_flag_bytes(int f, int m, int n) {
     return static_cast<size_t>(kMaxGrid) * 4 * sizeof(uint32_t);
 }
 inline size_t round256(size_t bytes) { return (bytes + 255) / 256 * 256; }
+// The grouping the deduplicating call from ids keeps in the workspace for a pass of S >
+// kMaxFusedSlots slots: the count, up to N experts, N + 1 offsets and the S-entry slot order.
+inline size_t dedup_grouping_bytes(int N, int S) { return round256(static_cast<size_t>(4) * (2 * N + S + 2)); }
 // The workspace's flag region: its size does not depend on the pass (the partial sums follow it).
 inline size_t expert_tc_flag_region(int f, int m) { return round256(expert_tc_flag_bytes(f, m, kMaxPassTokens)); }
 cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, uint64_t *part, cudaStream_t s,

@@ -20,6 +20,7 @@ namespace {
 
 constexpr int kSimtThreads = 256;
 constexpr int kSimtWarps = kSimtThreads / 32;
+constexpr int kWin = 16;   // tokens per window of accumulators
 
 template <typename T>
 __device__ __forceinline__ float ld_val(const T *p);
@@ -42,7 +43,7 @@ __global__ void __launch_bounds__(kSimtThreads) expert_simt_kernel(ExpertArgs a)
     __shared__ float s_h[kMaxPassTokens][kFTile];
     __shared__ float s_gate[kMaxPassTokens];
     __shared__ int s_expert;
-    __shared__ uint32_t s_mask;
+    __shared__ uint64_t s_mask;
 
     pdl_wait();
     const int tile = blockIdx.x;
@@ -51,13 +52,13 @@ __global__ void __launch_bounds__(kSimtThreads) expert_simt_kernel(ExpertArgs a)
 
     if (threadIdx.x == 0) {
         int e = -1;
-        uint32_t mask = 0;
+        uint64_t mask = 0;
         for (int t = 0; t < kMaxPassTokens; ++t) s_gate[t] = 0.0f;
         if (a.mode == kModePerSlot) {
             e = a.ids[g];
             const int t = g / a.m;
             s_gate[t] = a.gates[g];
-            mask = 1u << t;
+            mask = 1ull << t;
         } else if (g < a.num_distinct[0]) {   // g < min(N, n*m) by the launch shape
             e = a.expert_list[g];
             const int S = a.n * a.m;   // offsets are clamped to the slot buffer
@@ -67,7 +68,7 @@ __global__ void __launch_bounds__(kSimtThreads) expert_simt_kernel(ExpertArgs a)
                 const int t = slot / a.m;
                 if (slot >= 0 && t < a.n) {
                     s_gate[t] += a.gates[slot];
-                    mask |= 1u << t;
+                    mask |= 1ull << t;
                 }
             }
         } else {
@@ -82,7 +83,7 @@ __global__ void __launch_bounds__(kSimtThreads) expert_simt_kernel(ExpertArgs a)
     }
     __syncthreads();
     const int e = s_expert;
-    const uint32_t mask = s_mask;
+    const uint64_t mask = s_mask;
     if (e < 0) {
         pdl_trigger();
         return;
@@ -94,29 +95,34 @@ __global__ void __launch_bounds__(kSimtThreads) expert_simt_kernel(ExpertArgs a)
     const WT *wd = static_cast<const WT *>(a.w_down) + static_cast<size_t>(e) * d * f + i0;
     const XT *x = static_cast<const XT *>(a.x);
 
-    // gate/up rows of this tile: warp w takes rows w, w + 8, ...
+    // gate/up rows of this tile: warp w takes rows w, w + 8, ...; the group's tokens in
+    // windows of 16 (a window's rows are read again from cache, not from memory)
     for (int r = warp; r < kFTile; r += kSimtWarps) {
-        float gacc[kMaxPassTokens], uacc[kMaxPassTokens];
+        for (int t0 = 0; t0 < kMaxPassTokens; t0 += kWin) {
+            const uint32_t wm = static_cast<uint32_t>(mask >> t0) & 0xFFFFu;
+            if (wm == 0u) continue;
+            float gacc[kWin], uacc[kWin];
 #pragma unroll
-        for (int t = 0; t < kMaxPassTokens; ++t) { gacc[t] = 0.0f; uacc[t] = 0.0f; }
-        for (int k = lane; k < d; k += 32) {
-            const float wgv = ld_val<WT>(wg + static_cast<size_t>(r) * d + k);
-            const float wuv = ld_val<WT>(wu + static_cast<size_t>(r) * d + k);
+            for (int t = 0; t < kWin; ++t) { gacc[t] = 0.0f; uacc[t] = 0.0f; }
+            for (int k = lane; k < d; k += 32) {
+                const float wgv = ld_val<WT>(wg + static_cast<size_t>(r) * d + k);
+                const float wuv = ld_val<WT>(wu + static_cast<size_t>(r) * d + k);
 #pragma unroll
-            for (int t = 0; t < kMaxPassTokens; ++t) {
-                if ((mask >> t) & 1u) {
-                    const float xv = ld_val<XT>(x + static_cast<size_t>(t) * d + k);
-                    gacc[t] = fmaf(wgv, xv, gacc[t]);
-                    uacc[t] = fmaf(wuv, xv, uacc[t]);
+                for (int t = 0; t < kWin; ++t) {
+                    if ((wm >> t) & 1u) {
+                        const float xv = ld_val<XT>(x + static_cast<size_t>(t0 + t) * d + k);
+                        gacc[t] = fmaf(wgv, xv, gacc[t]);
+                        uacc[t] = fmaf(wuv, xv, uacc[t]);
+                    }
                 }
             }
-        }
 #pragma unroll
-        for (int t = 0; t < kMaxPassTokens; ++t) {
-            if ((mask >> t) & 1u) {
-                const float gs = warp_sum(gacc[t]);
-                const float us = warp_sum(uacc[t]);
-                if (lane == 0) s_h[t][r] = silu(gs) * us;
+            for (int t = 0; t < kWin; ++t) {
+                if ((wm >> t) & 1u) {
+                    const float gs = warp_sum(gacc[t]);
+                    const float us = warp_sum(uacc[t]);
+                    if (lane == 0) s_h[t0 + t][r] = silu(gs) * us;
+                }
             }
         }
     }
@@ -126,11 +132,15 @@ __global__ void __launch_bounds__(kSimtThreads) expert_simt_kernel(ExpertArgs a)
     for (int o = warp; o < d; o += kSimtWarps) {
         const float w0 = ld_val<WT>(wd + static_cast<size_t>(o) * f + lane);
         const float w1 = ld_val<WT>(wd + static_cast<size_t>(o) * f + lane + 32);
+        for (int t0 = 0; t0 < kMaxPassTokens; t0 += kWin) {
+            const uint32_t wm = static_cast<uint32_t>(mask >> t0) & 0xFFFFu;
+            if (wm == 0u) continue;
 #pragma unroll
-        for (int t = 0; t < kMaxPassTokens; ++t) {
-            if ((mask >> t) & 1u) {
-                const float p = warp_sum(w0 * s_h[t][lane] + w1 * s_h[t][lane + 32]);
-                if (lane == 0) atomicAdd(a.y + static_cast<size_t>(t) * d + o, s_gate[t] * p);
+            for (int t = 0; t < kWin; ++t) {
+                if ((wm >> t) & 1u) {
+                    const float p = warp_sum(w0 * s_h[t0 + t][lane] + w1 * s_h[t0 + t][lane + 32]);
+                    if (lane == 0) atomicAdd(a.y + static_cast<size_t>(t0 + t) * d + o, s_gate[t0 + t] * p);
+                }
             }
         }
     }

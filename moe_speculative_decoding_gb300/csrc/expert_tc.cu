@@ -16,23 +16,27 @@
 //
 //   gate/up blocks.  A gate/up item is (group, 64-row tile of f); its block is one k slice:
 //   64 rows of W_gate and the same 64 rows of W_up (16 KB, the M = 128 operand) plus the
-//   pass's x for that slice (16 tokens, from L2).  All G*T*KB blocks are cut into equal
+//   pass's x for that slice (NT tokens, from L2).  All G*T*KB blocks are cut into equal
 //   contiguous ranges, one per CTA, so every SM streams the same weight bytes whatever the
 //   pass size and the number of groups.  A CTA accumulates the blocks of each item it
-//   touches in TMEM (weights as M, tokens as N = 16, fp32) and stores the partial sums of
+//   touches in TMEM (weights as M, tokens as N = NT, fp32) and stores the partial sums of
 //   its share of the item to the workspace; with at most 2*G*T sharing CTAs an item meets
-//   at most three of them.  Each epilogue warp then publishes its part with a gpu-scope
-//   release flag that carries the call's ticket.
+//   at most three of them.  Each partial sum is stored as one 64-bit word together with the
+//   call's ticket, so the value is its own flag.
 //
 //   down blocks.  A down item is (group, two consecutive f tiles); its block is (item,
 //   128-row block of d, tile): 128 rows of W_down by 64 columns (16 KB).  The blocks are
 //   again cut into equal ranges.  The producer moves on to them as soon as its gate/up
 //   blocks are issued, so the ring fills with W_down while the last gate/up sums are
-//   formed elsewhere.  The h formers wait for the flags of the item's gate/up shares and form
-//   h = silu(g) * u from their partial sums in a fixed order, as the B operand in its
+//   formed elsewhere.  The h formers wait until the item's gate/up partial sums carry the
+//   call's ticket and form h = silu(g) * u from them in a fixed order, as the B operand in its
 //   swizzled layout (a large group's tokens split over up to four warps, each a round of
 //   dependent L2 loads fewer), and the epilogue adds gate * (W_down h) into the fp32 output with
 //   atomics: the weighted combine and the reduction over f tiles are fused there.
+//
+// The token width NT is 16 for passes of up to 16 tokens, 32 up to 32 and 64 above (the
+// deduplicating forms, where a group may hold every token of the pass): the same kernel with
+// NT-column accumulators, wider token masks and each warp's token table in shared memory.
 //
 // FP8 layers (e4m3 weights and x, one fp32 scale per weight row and per token) use the same
 // kernel instantiated for kind::f8f6f4: a 128-byte row then holds 128 elements, so a
@@ -61,52 +65,107 @@ constexpr int kThreads = 320;                 // warps: producer, MMA, 4 epilogu
 constexpr int kWarps = kThreads / 32;
 constexpr int kHWarps = kWarps - 6;           // h-former warps (6 ..)
 constexpr int kOB = 128;                      // d rows per down block
-constexpr int kNT = 16;                       // MMA N (token columns)
 constexpr uint32_t kWBytes = 16384;           // weight bytes of one block
-constexpr uint32_t kXTileBytes = kNT * 128;   // x of one k slice: 16 rows x 128 B
-constexpr uint32_t kSlotBytes = kWBytes + kXTileBytes;   // a ring slot: gate/up block + x, or down block
-// ring slots: 8 keeps enough copies in flight for the full stream (about 130 KB per SM) while
-// every dependent round trip waits behind fewer of them (11 and 6 measured slower)
-constexpr int kStages = 8;
-constexpr int kDownBufs = 8;                  // TMEM ring of down-block accumulators
-constexpr int kEpiBatch = 4;                  // down blocks per epilogue round
-constexpr int kHRing = 4;
 constexpr int kUnit = 2;                      // down blocks per TMEM accumulator (a unit)
-constexpr uint32_t kHBytes = kNT * 128;       // one h tile: 16 rows x 128 B
-constexpr uint32_t kHEntry = kUnit * kHBytes;
-constexpr uint32_t kInfoBytes = 144;          // mask, the 16 gates, the 16 h scales (FP8)
-constexpr int kGuBufs = 4;                    // TMEM ring of gate/up item accumulators
-constexpr uint32_t kTmemCols = 256;           // gate/up accumulators at columns 0-63, down at 64-191
-constexpr uint32_t kDnCol0 = 16 * kGuBufs;
 constexpr long long kDrainCycles = 400000000ll;   // about 0.2 s
-
-// Shared memory: the ring, kHRing h entries, their group records, each epilogue warp's copy
-// of the token scales (FP8), then barriers full[S], empty[S], gacc_full[G], gacc_empty[G],
-// dacc_full[B], dacc_empty[B], h_full[R], h_empty[R], drain, then the misc words.
-constexpr uint32_t kHOff = kStages * kSlotBytes;
-constexpr uint32_t kInfoOff = kHOff + kHRing * kHEntry;
-constexpr uint32_t kSxOff = kInfoOff + kHRing * kInfoBytes;
-constexpr uint32_t kBarOff = kSxOff + 4 * kNT * 4;
-constexpr int kNumBars = 2 * kStages + 2 * kGuBufs + 2 * kDownBufs + 2 * kHRing + 1;
-constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
 // the grouping of the deduplicating form from ids: expert list, offsets, slot order, the count,
-// two scan scratch rows, a copy of the ids, then the per-expert counts (N <= 1024)
-constexpr uint32_t kGrpOff = kMiscOff + 16;
+// two scan scratch rows, a copy of the ids (then the per-expert counts, N <= 1024)
 constexpr uint32_t kGrpWords = 3 * kMaxFusedSlots + 1 + 1 + 2 * kWarps + kMaxFusedSlots;
-constexpr uint32_t kCntOff = kGrpOff + ((kGrpWords * 4 + 15) & ~15u);
-constexpr uint32_t kSmem = kCntOff + 1024 * 4 + 1024;   // + alignment slack of the base
-static_assert(kSlotBytes % 1024 == 0 && kHOff % 1024 == 0 && kHEntry % 1024 == 0, "128-byte swizzle atoms");
-static_assert(kBarOff % 8 == 0, "mbarrier alignment");
-static_assert(kSmem <= 232448, "shared memory of one CTA");
-static_assert(4 * kThreads >= 1024 && kThreads >= kMaxFusedSlots && kHWarps >= 1 && kHWarps <= kNT,
-              "grouping bins and slots, h-former warps");
-static_assert(kDnCol0 + 16 * kDownBufs <= kTmemCols, "TMEM columns");
+
+// Token width NT of an instantiation: the MMA N, the rows of an x or h tile and the TMEM
+// columns of an accumulator.  16 serves passes of up to 16 tokens; 32 and 64 serve the
+// deduplicating forms up to 32 and 64 tokens, where one group can hold every token of the
+// pass.  A weight block stays 16 KB, but the x tile that rides with it and the h tiles grow
+// with NT, so the wide forms keep a ring as deep as shared memory allows: a slot is held
+// from its copy's issue until its MMAs complete, and the copies in flight per SM must cover
+// the memory latency at the stream's rate.
+//
+// The h ring needs no entry per h-former warp.  Its producers are kHWarps warps that each
+// form only some runs, so with fewer entries than warps a warp that waited only for its own
+// runs could pass an entry's parity wait a whole phase early (its last wait ordered it after
+// the release of run r' - kHRing with r' >= r - kHWarps, while the wait for run r is exact
+// only after the release of run r - 2 * kHRing).  A form with kHRing < kHWarps therefore
+// has every h-former warp wait for every run's entry in order, also for the runs it skips:
+// each wait then follows the one a phase before it, and none costs more than the entry's
+// reuse requires anyway.
+template <int NT>
+struct Cfg;
+template <>
+struct Cfg<16> {
+    // ring slots: 8 keeps enough copies in flight for the full stream (about 130 KB per SM)
+    // while every dependent round trip waits behind fewer of them (11 and 6 measured slower)
+    static constexpr int kStages = 8;
+    static constexpr int kDownBufs = 8;       // TMEM ring of down-block accumulators
+    static constexpr int kEpiBatch = 4;       // down accumulators per epilogue round
+    static constexpr int kHRing = 4;          // h entries (one per down run in flight)
+    static constexpr int kGuBufs = 4;         // TMEM ring of gate/up item accumulators
+    static constexpr uint32_t kTmemCols = 256;
+    using Mask = uint32_t;                    // a group's tokens
+};
+template <>
+struct Cfg<32> {
+    static constexpr int kStages = 8;
+    static constexpr int kDownBufs = 8;
+    static constexpr int kEpiBatch = 4;
+    static constexpr int kHRing = 4;
+    static constexpr int kGuBufs = 4;
+    static constexpr uint32_t kTmemCols = 512;
+    using Mask = uint32_t;
+};
+template <>
+struct Cfg<64> {
+    static constexpr int kStages = 7;
+    static constexpr int kDownBufs = 6;
+    static constexpr int kEpiBatch = 2;
+    static constexpr int kHRing = 2;
+    static constexpr int kGuBufs = 2;
+    static constexpr uint32_t kTmemCols = 512;
+    using Mask = uint64_t;
+};
+
+// Shared memory of an instantiation: the ring, kHRing h entries, their run records, each
+// epilogue warp's copy of the token scales (FP8) and of its run's gates, the token tables
+// of the wide form (below), then barriers full[S], empty[S], gacc_full[G], gacc_empty[G],
+// dacc_full[B], dacc_empty[B], h_full[R], h_empty[R], drain, the misc words, the in-kernel
+// grouping and the per-expert counts.
+template <int NT>
+struct Lay : Cfg<NT> {
+    using C = Cfg<NT>;
+    static constexpr uint32_t kXTileBytes = NT * 128;   // x of one k slice: NT rows x 128 B
+    static constexpr uint32_t kSlotBytes = kWBytes + kXTileBytes;   // gate/up block + x, or down block
+    static constexpr uint32_t kHBytes = NT * 128;       // one h tile: NT rows x 128 B
+    static constexpr uint32_t kHEntry = kUnit * kHBytes;
+    // a run record: the token mask (2 words), the NT gates, the NT h scales (FP8)
+    static constexpr uint32_t kInfoBytes = ((2 + 2 * NT) * 4 + 15) & ~15u;
+    static constexpr uint32_t kDnCol0 = NT * C::kGuBufs;   // gate/up accumulators first, then down
+    static constexpr uint32_t kHOff = C::kStages * kSlotBytes;
+    static constexpr uint32_t kInfoOff = kHOff + C::kHRing * kHEntry;
+    static constexpr uint32_t kSxOff = kInfoOff + C::kHRing * kInfoBytes;
+    static constexpr uint32_t kGwOff = kSxOff + 4 * NT * 4;
+    // wide form: slot positions and summed gates of the current group of each epilogue and
+    // h-former warp (the 16-token form keeps them in registers)
+    static constexpr uint32_t kTabOff = kGwOff + 4 * NT * 4;
+    static constexpr uint32_t kTabBytes = NT == 16 ? 0u : 8u * NT * 8u;
+    static constexpr uint32_t kBarOff = kTabOff + kTabBytes;
+    static constexpr int kNumBars = 2 * C::kStages + 2 * C::kGuBufs + 2 * C::kDownBufs + 2 * C::kHRing + 1;
+    static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
+    static constexpr uint32_t kGrpOff = kMiscOff + 16;
+    static constexpr uint32_t kCntOff = kGrpOff + ((kGrpWords * 4 + 15) & ~15u);
+    static constexpr uint32_t kSmem = kCntOff + 1024 * 4 + 1024;   // + alignment slack of the base
+    static_assert(kSlotBytes % 1024 == 0 && kHOff % 1024 == 0 && kHEntry % 1024 == 0, "128-byte swizzle atoms");
+    static_assert(kBarOff % 8 == 0, "mbarrier alignment");
+    static_assert(kSmem <= 232448, "shared memory of one CTA");
+    static_assert(4 * kThreads >= 1024 && kThreads >= kMaxFusedSlots && kHWarps >= 1 && kHWarps <= NT,
+                  "grouping bins and slots, h-former warps");
+    static_assert(kDnCol0 + NT * C::kDownBufs <= C::kTmemCols, "TMEM columns");
+    static_assert(NT % 16 == 0 && NT <= 64 && sizeof(typename C::Mask) * 8 >= NT, "token width");
+};
 
 // Element type of a kernel instantiation: bf16 (kind::f16) or e4m3 (kind::f8f6f4).
-template <bool F8>
+template <bool F8, int NT>
 struct Elt {
     static constexpr int BK = F8 ? 128 : 64;   // k elements per 128-byte row of an operand tile
-    static constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(128, kNT) : idesc_bf16_f32(128, kNT);
+    static constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(128, NT) : idesc_bf16_f32(128, NT);
     // a down block spans TPB 64-row gate/up tiles of f (one 128-byte row of W_down: 64 bf16 or
     // 128 e4m3), a unit kUnit blocks, a down item ITEM tiles: 128 f (bf16) or 256 f (e4m3)
     static constexpr int TPB = F8 ? 2 : 1;
@@ -170,16 +229,25 @@ __device__ __forceinline__ Seg seg_at(const ExpertArgs &a, long long b, long lon
 // Tokens of group g, computed by one whole warp: the mask of pass tokens in the group,
 // each token's summed gate and its slot position p (its row of the partial-sum buffer).
 // The deduplicating form reads the group's slot list with one lane per slot and gathers
-// it with ballots, so a group of k slots costs one round trip to memory, not k.
+// it with ballots, so a group of k slots costs one round trip to memory, not k.  The
+// 16-token form keeps the gates and positions in registers; the wide form in a table of
+// the warp's own in shared memory (gt and pos point there).
+template <int NT>
 struct GroupInfo {
+    typename Cfg<NT>::Mask mask;
+    float *gt;
+    int *pos;
+};
+template <>
+struct GroupInfo<16> {
     uint32_t mask;
-    float gt[kNT];
-    int pos[kNT];
+    float gt[16];
+    int pos[16];
 };
 
-__device__ __forceinline__ void group_tokens(const ExpertArgs &a, int g, int lane, GroupInfo &gi) {
+__device__ __forceinline__ void group_tokens(const ExpertArgs &a, int g, int lane, GroupInfo<16> &gi) {
 #pragma unroll
-    for (int t = 0; t < kNT; ++t) {
+    for (int t = 0; t < 16; ++t) {
         gi.gt[t] = 0.0f;
         gi.pos[t] = 0;
     }
@@ -187,7 +255,7 @@ __device__ __forceinline__ void group_tokens(const ExpertArgs &a, int g, int lan
         const int tt = g / a.m;
         const float gv = a.gates[g];
 #pragma unroll
-        for (int t = 0; t < kNT; ++t)
+        for (int t = 0; t < 16; ++t)
             if (t == tt) {
                 gi.gt[t] = gv;
                 gi.pos[t] = g;
@@ -210,7 +278,7 @@ __device__ __forceinline__ void group_tokens(const ExpertArgs &a, int g, int lan
             }
         }
 #pragma unroll
-        for (int t = 0; t < kNT; ++t) {
+        for (int t = 0; t < 16; ++t) {
             uint32_t bal = __ballot_sync(kFull, tt == t);
             if (bal == 0u) continue;
             mask |= 1u << t;
@@ -224,6 +292,65 @@ __device__ __forceinline__ void group_tokens(const ExpertArgs &a, int g, int lan
             }
             gi.gt[t] += sum;
         }
+    }
+    gi.mask = mask;
+}
+
+// The wide form: lanes holding the same token find each other with one match instead of a
+// ballot per token; the highest of them keeps the token's position and the gates' sum (in
+// ascending lane order, as above).  Only the mask's entries of the table are written.
+template <int NT>
+__device__ __forceinline__ void group_tokens(const ExpertArgs &a, int g, int lane, GroupInfo<NT> &gi) {
+    using Mask = typename Cfg<NT>::Mask;
+    __syncwarp();   // every lane has read the previous group's table
+    if (a.mode == kModePerSlot) {
+        const int tt = g / a.m;
+        if (lane == 0) {
+            gi.gt[tt] = a.gates[g];
+            gi.pos[tt] = g;
+        }
+        gi.mask = static_cast<Mask>(1) << tt;
+        __syncwarp();
+        return;
+    }
+    const int S = a.n * a.m;   // offsets are clamped to the slot buffer; slot < S gives token < n <= NT
+    const int p0 = max(0, a.offsets[g]), p1 = min(S, a.offsets[g + 1]);
+    Mask mask = 0;
+    for (int pb = p0; pb < p1; pb += 32) {
+        const int p = pb + lane;
+        int tt = -1;
+        float gv = 0.0f;
+        if (p < p1) {
+            const int slot = a.slot_order[p];
+            if (slot >= 0 && slot < S) {
+                tt = slot / a.m;
+                gv = a.gates[slot];
+            }
+        }
+        const uint32_t peers = __match_any_sync(kFull, tt >= 0 ? tt : -1 - lane);
+        const int rounds = static_cast<int>(__reduce_max_sync(kFull, static_cast<uint32_t>(__popc(peers))));
+        float sum = 0.0f;
+        uint32_t rest = peers;
+        for (int r = 0; r < rounds; ++r) {
+            const float v = __shfl_sync(kFull, gv, rest ? __ffs(rest) - 1 : lane);
+            if (rest) {
+                sum += v;
+                rest &= rest - 1u;
+            }
+        }
+        if (tt >= 0 && lane == 31 - __clz(peers)) {
+            const bool again = (mask >> tt) & 1u;   // a repeated token met in an earlier round
+            gi.gt[tt] = again ? gi.gt[tt] + sum : sum;
+            gi.pos[tt] = p;
+        }
+        const uint32_t lo = __reduce_or_sync(kFull, tt >= 0 && tt < 32 ? 1u << tt : 0u);
+        if constexpr (sizeof(Mask) == 8) {
+            const uint32_t hi = __reduce_or_sync(kFull, tt >= 32 ? 1u << (tt - 32) : 0u);
+            mask |= (static_cast<uint64_t>(hi) << 32) | lo;
+        } else {
+            mask |= lo;
+        }
+        __syncwarp();
     }
     gi.mask = mask;
 }
@@ -263,8 +390,23 @@ __device__ __forceinline__ uint32_t call_ticket(const uint32_t *sync) {
     return t == 0u ? 1u : t;
 }
 
-// The k-th token (ascending) of a token mask, or a value >= 16 when it has fewer.
+// The k-th token (ascending) of a token mask, or a value >= 64 when it has fewer.
 __device__ __forceinline__ uint32_t nth_token(uint32_t mask, int k) { return __fns(mask, 0u, k + 1); }
+__device__ __forceinline__ uint32_t nth_token(uint64_t mask, int k) {
+    const uint32_t lo = static_cast<uint32_t>(mask);
+    const int nl = __popc(lo);
+    if (k < nl) return __fns(lo, 0u, k + 1);
+    const uint32_t r = __fns(static_cast<uint32_t>(mask >> 32), 0u, k - nl + 1);
+    return r == 0xFFFFFFFFu ? r : 32u + r;
+}
+__device__ __forceinline__ int mask_count(uint32_t mask) { return __popc(mask); }
+__device__ __forceinline__ int mask_count(uint64_t mask) { return __popcll(mask); }
+// The token mask of a run record (words 0 and 1).
+template <typename Mask>
+__device__ __forceinline__ Mask run_mask(const uint32_t *rec) {
+    if constexpr (sizeof(Mask) == 4) return rec[0];
+    else return static_cast<uint64_t>(rec[0]) | (static_cast<uint64_t>(rec[1]) << 32);
+}
 
 // The grouping of the deduplicating form (the counting sort of moe_group_slots): experts in
 // ascending order with their slot offsets, slots of an expert in ascending order; ids outside
@@ -356,11 +498,19 @@ __device__ void build_grouping(const ExpertArgs &a, int my_id, int32_t *lst, int
 
 // ==================================================================== the kernel
 
-template <bool F8>
+template <bool F8, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
 expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
                  const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_x,
                  const ExpertArgs a, uint64_t *const part, const int zero_y) {
+    using L = Lay<NT>;
+    using Mask = typename L::Mask;
+    constexpr int kStages = L::kStages, kDownBufs = L::kDownBufs, kEpiBatch = L::kEpiBatch;
+    constexpr int kHRing = L::kHRing, kGuBufs = L::kGuBufs;
+    constexpr uint32_t kSlotBytes = L::kSlotBytes, kHBytes = L::kHBytes, kHEntry = L::kHEntry;
+    constexpr uint32_t kInfoBytes = L::kInfoBytes, kDnCol0 = L::kDnCol0, kTmemCols = L::kTmemCols;
+    constexpr uint32_t kHOff = L::kHOff, kInfoOff = L::kInfoOff, kBarOff = L::kBarOff, kMiscOff = L::kMiscOff;
+    constexpr int kRoundUnroll = NT == 16 ? 16 : 1;   // the h formers' rounds of token loads
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -475,11 +625,11 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     if (own_grouping) {
         ar.mode = kModePerSlot;
     } else if (a.mode == kModeDedupIds) {
-        int32_t *const grp = reinterpret_cast<int32_t *>(base_ptr + kGrpOff);
+        int32_t *const grp = reinterpret_cast<int32_t *>(base_ptr + L::kGrpOff);
         int32_t *const lst = grp, *const off = grp + kMaxFusedSlots, *const ord = grp + 2 * kMaxFusedSlots + 1;
         int32_t *const gcount = grp + 3 * kMaxFusedSlots + 1, *const scan = gcount + 1;
         int32_t *const ids_s = scan + 2 * kWarps;
-        build_grouping(a, my_id, lst, off, ord, reinterpret_cast<int32_t *>(base_ptr + kCntOff), gcount, scan, ids_s);
+        build_grouping(a, my_id, lst, off, ord, reinterpret_cast<int32_t *>(base_ptr + L::kCntOff), gcount, scan, ids_s);
         ar.mode = kModeDedup;
         ar.expert_list = lst;
         ar.offsets = off;
@@ -492,7 +642,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         st_release_gpu(a.sync, ticket);
     }
 
-    using E = Elt<F8>;
+    using E = Elt<F8, NT>;
     const int T = a.f / kFTile;
     const int KB = a.d / E::BK;
     const int G = num_groups(ar);
@@ -600,7 +750,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 break;
             }
             tc_fence_after();
-            const uint32_t d_tmem = tmem + 16u * buf;
+            const uint32_t d_tmem = tmem + NT * buf;
             for (long long bb = s.b0; bb < s.b1; ++bb) {
                 const uint32_t st = cnt % kStages, ph = (cnt / kStages) & 1u;
                 if (!warp_wait(bar_full + 8u * st, ph, abort_flag, a.err, wl)) {
@@ -658,7 +808,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                     if (elect_one()) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)   // 32 bytes of K per instruction
-                            E::mma(tmem + kDnCol0 + 16u * buf, desc_kmajor_sw128(sa + 32u * k),
+                            E::mma(tmem + kDnCol0 + NT * buf, desc_kmajor_sw128(sa + 32u * k),
                                    desc_kmajor_sw128(sbs + 32u * k), (sub != s0 || k != 0) ? 1u : 0u);
                         tc_commit(bar_empty + 8u * st);
                         if (sub == s1 - 1) tc_commit(bar_dacc_full + 8u * buf);
@@ -694,12 +844,18 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             if (lane == 0) st_release_gpu(a.flags + c * 4 + q, ticket);
         }
         // e4m3: this warp's copy of the token scales
-        float *const sxs = reinterpret_cast<float *>(base_ptr + kSxOff) + q * kNT;
+        float *const sxs = reinterpret_cast<float *>(base_ptr + L::kSxOff) + q * NT;
         if constexpr (F8) {
-            if (lane < kNT) sxs[lane] = lane < a.n ? a.s_x[lane] : 1.0f;
+            for (int t = lane; t < NT; t += 32) sxs[t] = t < a.n ? a.s_x[t] : 1.0f;
             __syncwarp();
         }
-        // gate/up: y_part[row, t] of each item share, then its flag
+        GroupInfo<NT> gi;
+        if constexpr (NT != 16) {
+            int *const tab = reinterpret_cast<int *>(base_ptr + L::kTabOff) + (warp - 2) * 2 * NT;
+            gi.pos = tab;
+            gi.gt = reinterpret_cast<float *>(tab + NT);
+        }
+        // gate/up: the partial sums [row, t] of each item share, tagged with the ticket
         uint32_t seg = 0;
         for (long long b = glo; b < ghi;) {
             const Seg s = seg_at(ar, b, ghi, KB, T);
@@ -716,7 +872,6 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 const int fr = s.e * a.f + s.tile * kFTile + (row & 63);
                 rs = row < 64 ? a.s_gate[fr] : a.s_up[fr];
             }
-            GroupInfo gi;
             group_tokens(ar, s.g, lane, gi);
             // this CTA's share of the item: 0 for the CTA holding its first block
             const int slot = c - gsp.part_of(static_cast<long long>(s.item) * KB);
@@ -728,20 +883,29 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 break;
             }
             tc_fence_after();
-            float v[16];
-            tmem_ld_16(tmem + lane_off + 16u * buf, v);
+            // 16 token columns at a time, only those holding a token of the group (the mask
+            // is the same in every lane); slot is in range with gu_parts' bound
+            if (slot >= 0 && slot < kMaxSpan) {
+#pragma unroll
+                for (int ch = 0; ch < NT / 16; ++ch) {
+                    const uint32_t cm = static_cast<uint32_t>(gi.mask >> (16 * ch)) & 0xFFFFu;
+                    if (cm == 0u) continue;
+                    float v[16];
+                    tmem_ld_16(tmem + lane_off + NT * buf + 16u * ch, v);
+                    if constexpr (F8) {
+                        // sums of code products back to values: weight-row scale times token scale
+#pragma unroll
+                        for (int t = 0; t < 16; ++t)
+                            if ((cm >> t) & 1u) v[t] *= rs * sxs[16 * ch + t];
+                    }
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        if ((cm >> t) & 1u)
+                            st_tagged(part + part_index(gi.pos[16 * ch + t], T, s.tile, slot, row), v[t], ticket);
+                }
+            }
             tc_fence_before();
             warp_arrive(bar_gacc_empty + 8u * buf);
-            if (slot < 0 || slot >= kMaxSpan) continue;   // not reachable with gu_parts' bound
-            if constexpr (F8) {
-                // sums of code products back to values: weight-row scale times token scale
-#pragma unroll
-                for (int t = 0; t < kNT; ++t)
-                    if ((gi.mask >> t) & 1u) v[t] *= rs * sxs[t];
-            }
-#pragma unroll
-            for (int t = 0; t < kNT; ++t)
-                if ((gi.mask >> t) & 1u) st_tagged(part + part_index(gi.pos[t], T, s.tile, slot, row), v[t], ticket);
         }
         // down: y[t, o] += gate_t * (W_down h)[o, t] with the run's gates from its group record
         if (ok && zero_y && dlo < dhi) {
@@ -758,14 +922,31 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             ++run;
             if (!warp_wait(bar_h_full + 8u * hb, hph, abort_flag, a.err, wl)) break;
             const uint32_t *const rec = reinterpret_cast<const uint32_t *>(info_ptr + hb * kInfoBytes);
-            const uint32_t mask = rec[0];
-            float gt[kNT];
+            const Mask mask = run_mask<Mask>(rec);
+            // the run's gates times the h scales of the span (written for the mask's tokens
+            // only): in registers (16 tokens) or in this warp's table (wide form), copied
+            // before the h entry is handed back
+            float gt[16];
+            float *const gw = reinterpret_cast<float *>(base_ptr + L::kGwOff) + q * NT;
+            if constexpr (NT == 16) {
 #pragma unroll
-            for (int t = 0; t < kNT; ++t) gt[t] = __uint_as_float(rec[1 + t]);
-            if constexpr (F8) {
+                for (int t = 0; t < 16; ++t) gt[t] = __uint_as_float(rec[2 + t]);
+                if constexpr (F8) {
 #pragma unroll
-                for (int t = 0; t < kNT; ++t)   // h scale of the span, written for the mask's tokens only
-                    if ((mask >> t) & 1u) gt[t] *= __uint_as_float(rec[17 + t]);
+                    for (int t = 0; t < 16; ++t)
+                        if ((mask >> t) & 1u) gt[t] *= __uint_as_float(rec[2 + NT + t]);
+                }
+            } else {
+                __syncwarp();   // every lane has read the previous run's gates
+                for (int t = lane; t < NT; t += 32) {
+                    float g = 0.0f;
+                    if ((mask >> t) & 1u) {
+                        g = __uint_as_float(rec[2 + t]);
+                        if constexpr (F8) g *= __uint_as_float(rec[2 + NT + t]);
+                    }
+                    gw[t] = g;
+                }
+                __syncwarp();
             }
             warp_arrive(bar_h_empty + 8u * hb);
             // e4m3: the W_down row scales of the next batch's units, loaded one batch ahead
@@ -777,7 +958,9 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 for (int j = 0; j < kEpiBatch; ++j) wsn[j] = (F8 && ob0 + j <= u.ob_last()) ? srow[(ob0 + j) * kOB] : 1.0f;
             };
             // units in batches of up to kEpiBatch (consecutive d blocks): their TMEM loads
-            // share one wait
+            // share one wait.  Token columns 16 at a time, those of the group only; the first
+            // 16 are loaded as each accumulator completes.
+            const uint32_t cm0 = static_cast<uint32_t>(mask) & 0xFFFFu;
             int ob = u.ob_first();
             while (ob <= u.ob_last() && u.s_lo(ob) >= u.s_hi(ob)) ++ob;   // no real sub-tile
             load_scales(ob);
@@ -799,28 +982,50 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                         break;
                     }
                     tc_fence_after();
-                    tmem_ld_16_async(tmem + kDnCol0 + lane_off + 16u * buf, r[j]);
+                    if (cm0 != 0u) tmem_ld_16_async(tmem + kDnCol0 + lane_off + NT * buf, r[j]);
                     ++nb;
                     ++dcnt;
                     ++ob;
                 }
                 tmem_wait_ld();   // also before leaving on an abort: no load stays in flight
                 if (!ok) break;
-                tc_fence_before();
-#pragma unroll
-                for (int j = 0; j < kEpiBatch; ++j)
-                    if (j < nb) warp_arrive(bar_dacc_empty + 8u * ((dcnt - nb + j) % kDownBufs));
-                if constexpr (F8) load_scales(ob);
                 const int ob0 = ob - nb;
 #pragma unroll
-                for (int j = 0; j < kEpiBatch; ++j) {
-                    if (j >= nb) break;
-                    const int o = (ob0 + j) * kOB + row;
-                    const float ws = wsc[j];   // W_down row scale (1 for bf16)
+                for (int ch = 0; ch < NT / 16; ++ch) {
+                    const uint32_t cm = ch == 0 ? cm0 : static_cast<uint32_t>(mask >> (16 * ch)) & 0xFFFFu;
+                    if (ch > 0 && cm != 0u) {
 #pragma unroll
-                    for (int t = 0; t < kNT; ++t)
-                        if ((mask >> t) & 1u)
-                            atomicAdd(a.y + static_cast<size_t>(t) * a.d + o, gt[t] * ws * __uint_as_float(r[j][t]));
+                        for (int j = 0; j < kEpiBatch; ++j)
+                            if (j < nb)
+                                tmem_ld_16_async(tmem + kDnCol0 + lane_off + NT * ((dcnt - nb + j) % kDownBufs) + 16u * ch,
+                                                 r[j]);
+                        tmem_wait_ld();
+                    }
+                    if (ch == NT / 16 - 1) {   // every column read: the accumulators are free
+                        tc_fence_before();
+#pragma unroll
+                        for (int j = 0; j < kEpiBatch; ++j)
+                            if (j < nb) warp_arrive(bar_dacc_empty + 8u * ((dcnt - nb + j) % kDownBufs));
+                        if constexpr (F8) load_scales(ob);
+                    }
+                    if (cm == 0u) continue;
+                    float g16[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        if constexpr (NT == 16) g16[t] = gt[t];
+                        else g16[t] = ((cm >> t) & 1u) ? gw[16 * ch + t] : 0.0f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < kEpiBatch; ++j) {
+                        if (j >= nb) break;
+                        const int o = (ob0 + j) * kOB + row;
+                        const float ws = wsc[j];   // W_down row scale (1 for bf16)
+#pragma unroll
+                        for (int t = 0; t < 16; ++t)
+                            if ((cm >> t) & 1u)
+                                atomicAdd(a.y + static_cast<size_t>(16 * ch + t) * a.d + o,
+                                          g16[t] * ws * __uint_as_float(r[j][t]));
+                    }
                 }
             }
         }
@@ -841,12 +1046,18 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         const int hw = warp - 6;
         // slot count of each group, clamped as group_tokens clamps the offsets (G <= N <= 1024;
         // the count area of the in-kernel grouping is free once it is built)
-        int32_t *const gcnt = reinterpret_cast<int32_t *>(base_ptr + kCntOff);
+        int32_t *const gcnt = reinterpret_cast<int32_t *>(base_ptr + L::kCntOff);
         if (ar.mode != kModePerSlot) {
             const int S = a.n * a.m;
             for (int g = hw * 32 + lane; g < G; g += kHWarps * 32)
                 gcnt[g] = max(0, min(S, ar.offsets[g + 1]) - max(0, ar.offsets[g]));
             named_barrier(2, kHWarps * 32);
+        }
+        GroupInfo<NT> gi;
+        if constexpr (NT != 16) {
+            int *const tab = reinterpret_cast<int *>(base_ptr + L::kTabOff) + (warp - 2) * 2 * NT;
+            gi.pos = tab;
+            gi.gt = reinterpret_cast<float *>(tab + NT);
         }
         uint32_t run = 0;
         for (long long b = dlo; b < dhi;) {
@@ -858,22 +1069,36 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             const int cnt = ar.mode == kModePerSlot ? 1 : gcnt[sg.g];
             const int nw = min(kHWarps, max(1, (cnt + E::TK - 1) / E::TK));   // warps forming the run
             const int first = (hw - static_cast<int>(rr % kHWarps) + kHWarps) % kHWarps;   // this warp's first token
-            if (first >= nw) continue;   // not a warp of this run
-            GroupInfo gi;
+            if (first >= nw) {   // not a warp of this run
+                if constexpr (kHRing < kHWarps) {
+                    // the entry's release in order with the others (see Cfg)
+                    if (!warp_wait(bar_h_empty + 8u * hb, hph ^ 1u, abort_flag, a.err, wl)) break;
+                }
+                continue;
+            }
             group_tokens(ar, sg.g, lane, gi);
             // this warp's tokens: every nw-th of the group's, from its first
-            uint32_t mymask = gi.mask;
+            Mask mymask = gi.mask;
             if (nw > 1) {
                 mymask = 0u;
-                int k = 0;
+                if constexpr (NT == 16) {
+                    int k = 0;
 #pragma unroll
-                for (int t = 0; t < kNT; ++t)
-                    if ((gi.mask >> t) & 1u) {
-                        if (k % nw == first) mymask |= 1u << t;
-                        ++k;
+                    for (int t = 0; t < 16; ++t)
+                        if ((gi.mask >> t) & 1u) {
+                            if (k % nw == first) mymask |= 1u << t;
+                            ++k;
+                        }
+                } else {
+                    Mask rest = gi.mask;
+                    for (int k = 0; rest != 0u; ++k) {
+                        const Mask low = rest & (~rest + 1u);   // the lowest remaining token
+                        if (k % nw == first) mymask |= low;
+                        rest ^= low;
                     }
+                }
             }
-            const int mine = __popc(mymask);
+            const int mine = mask_count(mymask);
             const int ntiles = min(E::ITEM, T - sg.tile * E::ITEM);   // real gate/up tiles of the item
             const int tile0 = sg.tile * E::ITEM;
             // the CTA shares of each real tile's gate/up item: first CTA and count
@@ -890,17 +1115,21 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             uint8_t *const hp = h_ptr + hb * kHEntry;
             uint32_t *const rec = reinterpret_cast<uint32_t *>(info_ptr + hb * kInfoBytes);
             // E::TK of this warp's tokens at a time: all loads first (predicated, independent)
-#pragma unroll
-            for (int k0 = 0; k0 < kNT; k0 += E::TK) {
+#pragma unroll kRoundUnroll
+            for (int k0 = 0; k0 < NT; k0 += E::TK) {
                 if (k0 >= mine) break;
                 uint32_t tk[E::TK];
                 int pk[E::TK];
 #pragma unroll
                 for (int j = 0; j < E::TK; ++j) {
-                    tk[j] = nth_token(mymask, k0 + j);   // >= 16 past the last
-                    pk[j] = 0;
+                    tk[j] = nth_token(mymask, k0 + j);   // >= NT past the last
+                    if constexpr (NT == 16) {
+                        pk[j] = 0;
 #pragma unroll
-                    for (int t = 0; t < kNT; ++t) pk[j] = (tk[j] == static_cast<uint32_t>(t)) ? gi.pos[t] : pk[j];
+                        for (int t = 0; t < 16; ++t) pk[j] = (tk[j] == static_cast<uint32_t>(t)) ? gi.pos[t] : pk[j];
+                    } else {
+                        pk[j] = tk[j] < static_cast<uint32_t>(NT) ? gi.pos[tk[j]] : 0;
+                    }
                 }
                 // the tagged partial sums of these tokens: all loads first (predicated,
                 // independent), then reloads of the words that do not carry this call's ticket
@@ -913,7 +1142,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
 #pragma unroll
                     for (int k = 0; k < E::COLS; ++k) {
                         const int c = lane + 32 * k, tl = c >> 6, i = c & 63;
-                        const bool on = tk[j] < static_cast<uint32_t>(kNT) && tl < ntiles;
+                        const bool on = tk[j] < static_cast<uint32_t>(NT) && tl < ntiles;
                         const uint64_t *const pp = part + part_index(pk[j], T, tile0 + (on ? tl : 0), 0, i);
 #pragma unroll
                         for (int sl = 0; sl < kMaxSpan; ++sl) {
@@ -948,7 +1177,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
 #pragma unroll
                         for (int k = 0; k < E::COLS; ++k) {
                             const int c = lane + 32 * k, tl = c >> 6, i = c & 63;
-                            const bool on = tk[j] < static_cast<uint32_t>(kNT) && tl < ntiles;
+                            const bool on = tk[j] < static_cast<uint32_t>(NT) && tl < ntiles;
                             const uint64_t *const pp = part + part_index(pk[j], T, tile0 + (on ? tl : 0), 0, i);
 #pragma unroll
                             for (int sl = 0; sl < kMaxSpan; ++sl) {
@@ -962,7 +1191,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
 #pragma unroll
                 for (int j = 0; j < E::TK; ++j) {
                     const uint32_t t = tk[j];
-                    if (t >= static_cast<uint32_t>(kNT)) break;
+                    if (t >= static_cast<uint32_t>(NT)) break;
                     float hv[E::COLS];
 #pragma unroll
                     for (int k = 0; k < E::COLS; ++k)
@@ -988,7 +1217,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
 #pragma unroll
                         for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
                         const float hs = mx > 0.0f ? mx / 448.0f : 1.0f;
-                        if (lane == 0) rec[17 + t] = __float_as_uint(hs);   // the token's h scale
+                        if (lane == 0) rec[2 + NT + t] = __float_as_uint(hs);   // the token's h scale
 #pragma unroll
                         for (int k = 0; k < E::COLS; ++k) {
                             const int c = lane + 32 * k, blk = c >> 7, fl = c & 127;   // block of 128, column in it
@@ -1003,10 +1232,20 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             if (!parts_ok) break;
             // the run's record (mask and gates) by the warp of its first token; the epilogue
             // reads the h scales of the mask's tokens only
-            if (first == 0 && lane == 0) {
-                rec[0] = gi.mask;
+            if (first == 0) {
+                if (lane == 0) {
+                    rec[0] = static_cast<uint32_t>(gi.mask);
+                    rec[1] = static_cast<uint32_t>(static_cast<uint64_t>(gi.mask) >> 32);
+                }
+                if constexpr (NT == 16) {
+                    if (lane == 0) {
 #pragma unroll
-                for (int t = 0; t < kNT; ++t) rec[1 + t] = __float_as_uint(gi.gt[t]);
+                        for (int t = 0; t < 16; ++t) rec[2 + t] = __float_as_uint(gi.gt[t]);
+                    }
+                } else {
+                    for (int t = lane; t < NT; t += 32)
+                        if ((gi.mask >> t) & 1u) rec[2 + t] = __float_as_uint(gi.gt[t]);
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -1067,20 +1306,20 @@ bool encode_2d(CUtensorMap *map, const void *ptr, bool bytes1, uint64_t inner, u
 
 struct DeviceInfo {
     int sms = 0;
-    bool attr_set[2] = {false, false};
+    bool attr_set[6] = {false, false, false, false, false, false};   // (e4m3, token width)
 };
 
 std::mutex g_info_mu;
 DeviceInfo g_info[64];
 
-template <bool F8>
+template <bool F8, int NT>
 cudaError_t set_attributes() {
-    return cudaFuncSetAttribute(expert_tc_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    return cudaFuncSetAttribute(expert_tc_kernel<F8, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<NT>::kSmem);
 }
 
-template <bool F8>
+template <bool F8, int NT>
 cudaError_t launch(const ExpertArgs &a, int sms, int max_groups, bool zero_y, uint64_t *part, cudaStream_t s, bool pdl) {
-    using E = Elt<F8>;
+    using E = Elt<F8, NT>;
     const long long T = a.f / kFTile, OBS = a.d / kOB;
     const long long T2 = (T + E::ITEM - 1) / E::ITEM;
     // CTAs with work: up to 2*G*T gate/up shares, and at most one per down block
@@ -1089,10 +1328,11 @@ cudaError_t launch(const ExpertArgs &a, int sms, int max_groups, bool zero_y, ui
 
     CUtensorMap tm_wg, tm_wu, tm_wd, tm_x;
     const uint64_t d = a.d, f = a.f, N = a.N;
+    // x: boxes of NT rows; the rows past the pass's n are filled with zeros
     if (!encode_2d(&tm_wg, a.w_gate, F8, d, N * f, E::BK, kFTile) ||
         !encode_2d(&tm_wu, a.w_up, F8, d, N * f, E::BK, kFTile) ||
         !encode_2d(&tm_wd, a.w_down, F8, f, N * d, E::BK, kOB) ||
-        !encode_2d(&tm_x, a.x, F8, d, static_cast<uint64_t>(a.n), E::BK, kNT))
+        !encode_2d(&tm_x, a.x, F8, d, static_cast<uint64_t>(a.n), E::BK, NT))
         return cudaErrorInvalidValue;
 
     cudaLaunchAttribute attr[1];
@@ -1101,11 +1341,11 @@ cudaError_t launch(const ExpertArgs &a, int sms, int max_groups, bool zero_y, ui
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmem;
+    cfg.dynamicSmemBytes = Lay<NT>::kSmem;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, expert_tc_kernel<F8>, tm_wg, tm_wu, tm_wd, tm_x, a, part, zero_y ? 1 : 0);
+    return cudaLaunchKernelEx(&cfg, expert_tc_kernel<F8, NT>, tm_wg, tm_wu, tm_wd, tm_x, a, part, zero_y ? 1 : 0);
 }
 
 }  // namespace
@@ -1116,12 +1356,16 @@ cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, u
                              bool pdl) {
     const bool f8 = a.w_dtype == MOE_E4M3 && a.x_dtype == MOE_E4M3;
     const bool bf = a.w_dtype == MOE_BF16 && a.x_dtype == MOE_BF16;
-    if (!expert_tc_supports(a.d, a.f) || !(f8 || bf) || a.n > kNT || max_groups < 1) return cudaErrorNotSupported;
+    if (!expert_tc_supports(a.d, a.f) || !(f8 || bf) || a.n < 1 || a.n > kMaxPassTokens || max_groups < 1)
+        return cudaErrorNotSupported;
     if (a.sync == nullptr || a.flags == nullptr) return cudaErrorInvalidValue;
     // e4m3: 128-element k slices; h spans of 256 f (the last may be 128)
     if (f8 && (a.d % 128 != 0 || a.f % 128 != 0 || a.s_gate == nullptr || a.s_up == nullptr ||
                a.s_down == nullptr || a.s_x == nullptr))
         return cudaErrorNotSupported;
+    // the token width: the narrowest instantiation that holds the pass
+    const int width = a.n <= 16 ? 0 : (a.n <= 32 ? 1 : 2);
+    const int form = (f8 ? 1 : 0) + 2 * width;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -1133,15 +1377,28 @@ cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, u
             err = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
             if (err != cudaSuccess) return err;
         }
-        if (!di.attr_set[f8 ? 1 : 0]) {
-            err = f8 ? set_attributes<true>() : set_attributes<false>();
+        if (!di.attr_set[form]) {
+            switch (form) {
+                case 0: err = set_attributes<false, 16>(); break;
+                case 1: err = set_attributes<true, 16>(); break;
+                case 2: err = set_attributes<false, 32>(); break;
+                case 3: err = set_attributes<true, 32>(); break;
+                case 4: err = set_attributes<false, 64>(); break;
+                default: err = set_attributes<true, 64>(); break;
+            }
             if (err != cudaSuccess) return err;
-            di.attr_set[f8 ? 1 : 0] = true;
+            di.attr_set[form] = true;
         }
         sms = di.sms;
     }
-    return f8 ? launch<true>(a, sms, max_groups, zero_y, part, s, pdl)
-              : launch<false>(a, sms, max_groups, zero_y, part, s, pdl);
+    switch (form) {
+        case 0: return launch<false, 16>(a, sms, max_groups, zero_y, part, s, pdl);
+        case 1: return launch<true, 16>(a, sms, max_groups, zero_y, part, s, pdl);
+        case 2: return launch<false, 32>(a, sms, max_groups, zero_y, part, s, pdl);
+        case 3: return launch<true, 32>(a, sms, max_groups, zero_y, part, s, pdl);
+        case 4: return launch<false, 64>(a, sms, max_groups, zero_y, part, s, pdl);
+        default: return launch<true, 64>(a, sms, max_groups, zero_y, part, s, pdl);
+    }
 }
 
 }  // namespace moe

@@ -56,7 +56,9 @@ extern "C" moe_status_t moe_expert_op_perslot_noalloc(const moe_layer_t *layer, 
     const moe_status_t checked = moe::check_perslot_call(layer, w_gate, w_up, w_down, x, ids, gates, n, y);
     if (checked != MOE_OK) return checked;
     if (status_out != nullptr && (reinterpret_cast<uintptr_t>(status_out) & 3u) != 0) return MOE_ERR_ARG;
-    if (moe_workspace_bytes(layer, n) > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
+    // the per-slot calls launch at most MOE_PERSLOT_LAUNCH_TOKENS tokens at a time
+    const int32_t nl = n < MOE_PERSLOT_LAUNCH_TOKENS ? n : MOE_PERSLOT_LAUNCH_TOKENS;
+    if (moe_workspace_bytes(layer, nl) > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
     void *ws = nullptr;
     if (scratch_address(&ws) != cudaSuccess) return MOE_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(s);

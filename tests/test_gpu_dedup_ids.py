@@ -103,11 +103,29 @@ def test_unsupported_shapes():
     gates = torch.ones((4, 2), device="cuda")
     with pytest.raises(api.MoeError):
         api.expert_op_dedup_ids(f32, dl.w, x, ids, gates, ws=dl.ws)
+    with pytest.raises(api.MoeError):   # above 64 tokens
+        bf = DeviceLayer(256, 128, 8, 2, "bf16", seed=734)
+        api.expert_op_dedup_ids(bf.layer, bf.w, bf.activations(65, seed=735),
+                                torch.zeros((65, 2), dtype=torch.int32, device="cuda"),
+                                torch.ones((65, 2), device="cuda"), ws=api.workspace(bf.layer, 64, "cuda"))
+
+
+def test_more_than_256_slots_group_in_the_workspace(oracle_mod):
+    """9 tokens of top-32: 288 slots, more than the kernel groups in shared memory, so the call
+    from ids groups them with moe_group_slots into the workspace first.  Every slot names expert
+    0 (one group of 9 tokens, each token's 32 gates added), then random routing."""
     big = DeviceLayer(256, 128, 64, 32, "bf16", seed=732)
-    xb = big.activations(9, seed=733)
-    with pytest.raises(api.MoeError):   # n m = 288 > 256
-        api.expert_op_dedup_ids(big.layer, big.w, xb, torch.zeros((9, 32), dtype=torch.int32, device="cuda"),
-                                torch.ones((9, 32), device="cuda"), ws=big.ws)
+    n = 9
+    xb = big.activations(n, seed=733)
+    rng = np.random.default_rng(736)
+    gates_np = rng.random((n, 32)).astype(np.float32)
+    gates = torch.from_numpy(gates_np).cuda()
+    for ids_np in (np.zeros((n, 32), np.int32), np.stack([rng.permutation(64)[:32] for _ in range(n)]).astype(np.int32)):
+        ids = torch.from_numpy(ids_np).cuda()
+        y = api.expert_op_dedup_ids(big.layer, big.w, xb, ids, gates, ws=big.ws).cpu().numpy()
+        assert api.last_device_error(big.ws) == 0
+        ref = oracle_mod.expert_op_perslot(*big.host(), synth.host_array(xb), ids_np, gates_np)
+        assert rel_max_err(y, ref) <= TOL_BF16
 
 
 def test_routing_slices_need_only_element_alignment(oracle_mod):

@@ -30,7 +30,7 @@ def test_exports_every_declared_symbol(lib):
     for name in declared:
         assert hasattr(lib, name), name
     assert set(declared) == set(api.EXPORTED)
-    assert lib.moe_abi_version() == 1
+    assert lib.moe_abi_version() == 2
 
 
 def test_status_strings(lib):
@@ -50,12 +50,16 @@ def test_argument_validation_before_any_launch(lib):
     bad = api.make_layer(2048, 700, 128, 8)   # f not a multiple of 64
     args = [None] * 6
     assert lib.moe_expert_op_perslot(ctypes.byref(bad), *args, 4, 0, None, None, 0, None) == 2
-    # n above the per-slot limit (64); 17..64 are taken as launches of up to 16 tokens, so here
-    # their null pointers are the error; the deduplicating form stops at 16
+    # n above the pass limit (64) is unsupported in every form; up to 64 the null pointers are
+    # the error (the per-slot calls split 17..64 into launches of up to 16 tokens, the
+    # deduplicating ones take them in one launch)
     assert lib.moe_expert_op_perslot(ctypes.byref(L), *args, 65, 0, None, None, 0, None) == 2
     assert lib.moe_expert_op_perslot(ctypes.byref(L), *args, 17, 0, None, None, 0, None) == 1
     assert lib.moe_expert_op_perslot(ctypes.byref(L), *args, 64, 0, None, None, 0, None) == 1
-    assert lib.moe_expert_op_dedup_ids(ctypes.byref(L), *args, 17, 0, None, None, 0, None) == 2
+    assert lib.moe_expert_op_dedup_ids(ctypes.byref(L), *args, 17, 0, None, None, 0, None) == 1
+    assert lib.moe_expert_op_dedup_ids(ctypes.byref(L), *args, 64, 0, None, None, 0, None) == 1
+    assert lib.moe_expert_op_dedup_ids(ctypes.byref(L), *args, 65, 0, None, None, 0, None) == 2
+    assert lib.moe_expert_op_dedup(ctypes.byref(L), *[None] * 5, 65, *[None] * 4, 0, None, None, 0, None) == 2
     # null pointers
     assert lib.moe_expert_op_perslot(ctypes.byref(L), *args, 4, 0, None, None, 0, None) == 1
     mixed = api.Layer(2048, 768, 128, 8, 1, 0, 0)   # bf16 weights with fp32 x
@@ -72,11 +76,14 @@ def test_workspace_bytes(lib):
     for (d, f, N, m) in [(2048, 768, 128, 8), (2048, 1408, 64, 6), (4096, 14336, 8, 2), (256, 128, 8, 2)]:
         L = api.make_layer(d, f, N, m, "bf16")
         flags = r256(256 * 4 * 4)
-        for n in (1, 5, 16):
+        for n in (1, 5, 16, 17, 40, 64):
             part = n * m * (f // 64) * 3 * 128 * 8
-            assert lib.moe_workspace_bytes(ctypes.byref(L), n) == 256 + flags + r256(part)
+            # a pass of more than 256 slots keeps its grouping (count, N ids, N + 1 offsets,
+            # n*m slots) for the deduplicating call from ids
+            grouping = r256(4 * (2 * N + n * m + 2)) if n * m > 256 else 0
+            assert lib.moe_workspace_bytes(ctypes.byref(L), n) == 256 + flags + r256(part) + grouping
         # passes cap at MOE_MAX_PASS_TOKENS
-        assert lib.moe_workspace_bytes(ctypes.byref(L), 64) == lib.moe_workspace_bytes(ctypes.byref(L), 16)
+        assert lib.moe_workspace_bytes(ctypes.byref(L), 100) == lib.moe_workspace_bytes(ctypes.byref(L), 64)
     assert lib.moe_workspace_bytes(ctypes.byref(api.make_layer(2048, 768, 128, 8)), 16) == 256 + 4096 + 4718592
     # the SIMT kernel and fp32 layers keep only the header
     assert lib.moe_workspace_bytes(ctypes.byref(api.make_layer(256, 512, 8, 2, "f32")), 16) == 256
