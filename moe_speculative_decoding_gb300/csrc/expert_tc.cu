@@ -736,7 +736,11 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        // Warp-uniform loop; waits by every lane, MMAs and commits by one elected lane.
+        // Warp-uniform loop; waits by every lane, MMAs and commits by one elected lane.  A
+        // round of waits and issue costs about as much as four MMAs of its own, so a round
+        // takes the next block of the same accumulator as well when its copy has already landed
+        // (a non-blocking test): eight MMAs back to back where the stream runs ahead of the
+        // issuer, and no wait added where the issuer waits for the stream.
         uint32_t cnt = 0, seg = 0;
         bool ok = true;
         for (long long b = glo; ok && b < ghi;) {
@@ -751,25 +755,33 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             }
             tc_fence_after();
             const uint32_t d_tmem = tmem + NT * buf;
-            for (long long bb = s.b0; bb < s.b1; ++bb) {
-                const uint32_t st = cnt % kStages, ph = (cnt / kStages) & 1u;
-                if (!warp_wait(bar_full + 8u * st, ph, abort_flag, a.err, wl)) {
+            for (long long bb = s.b0; bb < s.b1;) {
+                uint32_t st[2] = {cnt % kStages, (cnt + 1) % kStages};
+                if (!warp_wait(bar_full + 8u * st[0], (cnt / kStages) & 1u, abort_flag, a.err, wl)) {
                     ok = false;
                     break;
                 }
+                const int nbk = (s.b1 - bb >= 2 && __all_sync(kFull, mbar_test_wait(bar_full + 8u * st[1],
+                                                                                   ((cnt + 1) / kStages) & 1u)))
+                                    ? 2 : 1;   // blocks of this round
                 tc_fence_after();
-                const uint32_t sa = base + st * kSlotBytes;
-                const uint32_t sb = sa + kWBytes;
                 if (elect_one()) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)   // 32 bytes of K per instruction
-                        E::mma(d_tmem, desc_kmajor_sw128(sa + 32u * k), desc_kmajor_sw128(sb + 32u * k),
-                               (bb != s.b0 || k != 0) ? 1u : 0u);
-                    tc_commit(bar_empty + 8u * st);
-                    if (bb == s.b1 - 1) tc_commit(bar_gacc_full + 8u * buf);
+                    for (int j = 0; j < 2; ++j) {
+                        if (j >= nbk) break;
+                        const uint32_t sa = base + st[j] * kSlotBytes;
+                        const uint32_t sb = sa + kWBytes;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)   // 32 bytes of K per instruction
+                            E::mma(d_tmem, desc_kmajor_sw128(sa + 32u * k), desc_kmajor_sw128(sb + 32u * k),
+                                   (bb + j != s.b0 || k != 0) ? 1u : 0u);
+                        tc_commit(bar_empty + 8u * st[j]);   // each slot as soon as its own MMAs are done
+                    }
+                    if (bb + nbk == s.b1) tc_commit(bar_gacc_full + 8u * buf);
                 }
                 __syncwarp();
-                ++cnt;
+                cnt += nbk;
+                bb += nbk;
             }
         }
         uint32_t dcnt = 0, run = 0;
@@ -796,25 +808,34 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                     break;
                 }
                 tc_fence_after();
-                for (int sub = s0; sub < s1; ++sub) {
-                    const uint32_t st = cnt % kStages, ph = (cnt / kStages) & 1u;
-                    if (!warp_wait(bar_full + 8u * st, ph, abort_flag, a.err, wl)) {
+                // the unit's blocks (at most E::UNIT = 2), in rounds as above
+                for (int sub = s0; sub < s1;) {
+                    const uint32_t st[2] = {cnt % kStages, (cnt + 1) % kStages};
+                    if (!warp_wait(bar_full + 8u * st[0], (cnt / kStages) & 1u, abort_flag, a.err, wl)) {
                         ok = false;
                         break;
                     }
+                    const int nbk = (s1 - sub >= 2 && __all_sync(kFull, mbar_test_wait(bar_full + 8u * st[1],
+                                                                                      ((cnt + 1) / kStages) & 1u)))
+                                        ? 2 : 1;
                     tc_fence_after();
-                    const uint32_t sa = base + st * kSlotBytes;
-                    const uint32_t sbs = shb + static_cast<uint32_t>(sub) * kHBytes;
                     if (elect_one()) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)   // 32 bytes of K per instruction
-                            E::mma(tmem + kDnCol0 + NT * buf, desc_kmajor_sw128(sa + 32u * k),
-                                   desc_kmajor_sw128(sbs + 32u * k), (sub != s0 || k != 0) ? 1u : 0u);
-                        tc_commit(bar_empty + 8u * st);
-                        if (sub == s1 - 1) tc_commit(bar_dacc_full + 8u * buf);
+                        for (int j = 0; j < 2; ++j) {
+                            if (j >= nbk) break;
+                            const uint32_t sa = base + st[j] * kSlotBytes;
+                            const uint32_t sbs = shb + static_cast<uint32_t>(sub + j) * kHBytes;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)   // 32 bytes of K per instruction
+                                E::mma(tmem + kDnCol0 + NT * buf, desc_kmajor_sw128(sa + 32u * k),
+                                       desc_kmajor_sw128(sbs + 32u * k), (sub + j != s0 || k != 0) ? 1u : 0u);
+                            tc_commit(bar_empty + 8u * st[j]);
+                        }
+                        if (sub + nbk == s1) tc_commit(bar_dacc_full + 8u * buf);
                     }
                     __syncwarp();
-                    ++cnt;
+                    cnt += nbk;
+                    sub += nbk;
                 }
             }
             // the h entry is free again once this run's MMAs have read it
