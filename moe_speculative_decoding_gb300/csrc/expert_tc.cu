@@ -106,7 +106,7 @@ template <>
 struct Cfg<32> {
     static constexpr int kStages = 8;
     static constexpr int kDownBufs = 8;
-    static constexpr int kEpiBatch = 4;
+    static constexpr int kEpiBatch = 2;       // 2 x 32 columns: the registers of 4 x 16
     static constexpr int kHRing = 4;
     static constexpr int kGuBufs = 4;
     static constexpr uint32_t kTmemCols = 512;
@@ -116,7 +116,7 @@ template <>
 struct Cfg<64> {
     static constexpr int kStages = 7;
     static constexpr int kDownBufs = 6;
-    static constexpr int kEpiBatch = 2;
+    static constexpr int kEpiBatch = 1;
     static constexpr int kHRing = 2;
     static constexpr int kGuBufs = 2;
     static constexpr uint32_t kTmemCols = 512;
@@ -907,12 +907,19 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             // 16 token columns at a time, only those holding a token of the group (the mask
             // is the same in every lane); slot is in range with gu_parts' bound
             if (slot >= 0 && slot < kMaxSpan) {
+                uint32_t vr[NT / 16][16];
+#pragma unroll
+                for (int ch = 0; ch < NT / 16; ++ch)
+                    if ((static_cast<uint32_t>(gi.mask >> (16 * ch)) & 0xFFFFu) != 0u)
+                        tmem_ld_16_async(tmem + lane_off + NT * buf + 16u * ch, vr[ch]);
+                tmem_wait_ld();
 #pragma unroll
                 for (int ch = 0; ch < NT / 16; ++ch) {
                     const uint32_t cm = static_cast<uint32_t>(gi.mask >> (16 * ch)) & 0xFFFFu;
                     if (cm == 0u) continue;
                     float v[16];
-                    tmem_ld_16(tmem + lane_off + NT * buf + 16u * ch, v);
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(vr[ch][t]);
                     if constexpr (F8) {
                         // sums of code products back to values: weight-row scale times token scale
 #pragma unroll
@@ -981,13 +988,13 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             // units in batches of up to kEpiBatch (consecutive d blocks): their TMEM loads
             // share one wait.  Token columns 16 at a time, those of the group only; the first
             // 16 are loaded as each accumulator completes.
-            const uint32_t cm0 = static_cast<uint32_t>(mask) & 0xFFFFu;
+            constexpr int kCh = NT / 16;   // 16-column chunks of an accumulator
             int ob = u.ob_first();
             while (ob <= u.ob_last() && u.s_lo(ob) >= u.s_hi(ob)) ++ob;   // no real sub-tile
             load_scales(ob);
             while (ok && ob <= u.ob_last()) {
                 int nb = 0;
-                uint32_t r[kEpiBatch][16];
+                uint32_t r[kEpiBatch][kCh][16];
                 float wsc[kEpiBatch];
 #pragma unroll
                 for (int j = 0; j < kEpiBatch; ++j) {
@@ -1003,32 +1010,26 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                         break;
                     }
                     tc_fence_after();
-                    if (cm0 != 0u) tmem_ld_16_async(tmem + kDnCol0 + lane_off + NT * buf, r[j]);
+                    // every chunk that holds a token of the group, all behind one wait
+#pragma unroll
+                    for (int ch = 0; ch < kCh; ++ch)
+                        if ((static_cast<uint32_t>(mask >> (16 * ch)) & 0xFFFFu) != 0u)
+                            tmem_ld_16_async(tmem + kDnCol0 + lane_off + NT * buf + 16u * ch, r[j][ch]);
                     ++nb;
                     ++dcnt;
                     ++ob;
                 }
                 tmem_wait_ld();   // also before leaving on an abort: no load stays in flight
                 if (!ok) break;
+                tc_fence_before();
+#pragma unroll
+                for (int j = 0; j < kEpiBatch; ++j)
+                    if (j < nb) warp_arrive(bar_dacc_empty + 8u * ((dcnt - nb + j) % kDownBufs));
+                if constexpr (F8) load_scales(ob);
                 const int ob0 = ob - nb;
 #pragma unroll
-                for (int ch = 0; ch < NT / 16; ++ch) {
-                    const uint32_t cm = ch == 0 ? cm0 : static_cast<uint32_t>(mask >> (16 * ch)) & 0xFFFFu;
-                    if (ch > 0 && cm != 0u) {
-#pragma unroll
-                        for (int j = 0; j < kEpiBatch; ++j)
-                            if (j < nb)
-                                tmem_ld_16_async(tmem + kDnCol0 + lane_off + NT * ((dcnt - nb + j) % kDownBufs) + 16u * ch,
-                                                 r[j]);
-                        tmem_wait_ld();
-                    }
-                    if (ch == NT / 16 - 1) {   // every column read: the accumulators are free
-                        tc_fence_before();
-#pragma unroll
-                        for (int j = 0; j < kEpiBatch; ++j)
-                            if (j < nb) warp_arrive(bar_dacc_empty + 8u * ((dcnt - nb + j) % kDownBufs));
-                        if constexpr (F8) load_scales(ob);
-                    }
+                for (int ch = 0; ch < kCh; ++ch) {
+                    const uint32_t cm = static_cast<uint32_t>(mask >> (16 * ch)) & 0xFFFFu;
                     if (cm == 0u) continue;
                     float g16[16];
 #pragma unroll
@@ -1045,7 +1046,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                         for (int t = 0; t < 16; ++t)
                             if ((cm >> t) & 1u)
                                 atomicAdd(a.y + static_cast<size_t>(16 * ch + t) * a.d + o,
-                                          g16[t] * ws * __uint_as_float(r[j][t]));
+                                          g16[t] * ws * __uint_as_float(r[j][ch][t]));
                     }
                 }
             }
