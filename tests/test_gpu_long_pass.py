@@ -188,3 +188,47 @@ def test_cuda_core_kernel_long_dedup_pass(oracle_mod, dtype):
     assert api.last_device_error(ws) == 0
     ref = oracle_mod.expert_op_perslot(*dl.host(), synth.host_array(x), ids.cpu().numpy(), gates.cpu().numpy())
     assert rel_max_err(y, ref) <= (TOL_F32 if dtype == "f32" else TOL_BF16)
+
+
+def test_largest_pass_of_the_largest_routing(oracle_mod):
+    """The supported maxima of the routing side at once: N = 1024 experts, top-32, 64 tokens
+    (2,048 slots, grouped with moe_group_slots into the workspace), both deduplicating calls and
+    the per-slot call, sampled tokens against the oracle."""
+    d, f, N, m, n = 256, 128, 1024, 32, 64
+    dl = DeviceLayer(d, f, N, m, "bf16", seed=900)
+    ws = api.workspace(dl.layer, n, "cuda")
+    x = dl.activations(n, seed=901)
+    _, logits = synth.routing_traces(1, n, N, m, 0.4, seed=902)
+    ids, gates = route(logits[0], m)
+    y1 = api.expert_op_dedup_ids(dl.layer, dl.w, x, ids, gates, ws=ws).cpu().numpy()
+    grp = api.group_slots(ids, N, ws=ws)
+    y2 = api.expert_op_dedup(dl.layer, dl.w, x, gates, grp, ws=ws).cpu().numpy()
+    y3 = api.expert_op_perslot(dl.layer, dl.w, x, ids, gates, ws=ws).cpu().numpy()
+    assert api.last_device_error(ws) == 0
+    assert rel_max_err(y2, y1) <= 1e-4
+    ids_h, g_h = ids.cpu().numpy(), gates.cpu().numpy().astype(np.float64)
+    xh = synth.host_array(x)
+    local = np.arange(m, dtype=np.int32)[None, :].repeat(n, axis=0)
+    rows = {t: oracle_mod.expert_op_token(*dl.host_experts(ids_h[t]), xh, local, g_h, t) for t in (0, 21, 42, 63)}
+    _check_rows(y1, rows)
+    _check_rows(y3, rows)
+
+
+def test_largest_layer_dimensions(oracle_mod):
+    """d = 8192 and f = 65536, the largest the library takes (two experts of 3.2 GB each, top-1,
+    two tokens), both forms against the oracle on every token."""
+    d, f, N, m, n = 8192, 65536, 2, 1, 2
+    dl = DeviceLayer(d, f, N, m, "bf16", seed=910)
+    x = dl.activations(n, seed=911)
+    ids = torch.tensor([[1], [0]], dtype=torch.int32, device="cuda")
+    gates = torch.tensor([[0.75], [1.25]], device="cuda")
+    ws = api.workspace(dl.layer, n, "cuda")
+    ys = api.expert_op_perslot(dl.layer, dl.w, x, ids, gates, ws=ws).cpu().numpy()
+    yd = api.expert_op_dedup_ids(dl.layer, dl.w, x, ids, gates, ws=ws).cpu().numpy()
+    assert api.last_device_error(ws) == 0
+    ids_h, g_h = ids.cpu().numpy(), gates.cpu().numpy().astype(np.float64)
+    xh = synth.host_array(x)
+    local = np.zeros((n, 1), np.int32)
+    rows = {t: oracle_mod.expert_op_token(*dl.host_experts(ids_h[t]), xh, local, g_h, t) for t in range(n)}
+    _check_rows(ys, rows)
+    _check_rows(yd, rows)
