@@ -7,7 +7,7 @@
 
 namespace moe {
 
-constexpr int kMaxPassTokens = MOE_MAX_PASS_TOKENS;   // tokens per pass (MMA N = 16, or 64 above 16)
+constexpr int kMaxPassTokens = MOE_MAX_PASS_TOKENS;   // tokens per pass (MMA N = 16, 32 or 64)
 constexpr int kPerSlotLaunchTokens = MOE_PERSLOT_LAUNCH_TOKENS;   // tokens per launch of the per-slot calls
 constexpr int kFTile = 64;                             // rows of f per work item
 
