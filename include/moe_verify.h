@@ -81,11 +81,11 @@ typedef struct {
 
 /* Largest pass size (tokens per verification pass) every expert-operation call accepts. */
 #define MOE_MAX_PASS_TOKENS 64
-/* The per-slot calls run a pass above this many tokens as consecutive launches of up to this
- * many (the per-slot form reads every slot's expert either way), so their workspace needs
- * only moe_workspace_bytes(layer, MOE_PERSLOT_LAUNCH_TOKENS).  The deduplicating calls run a
- * pass of up to MOE_MAX_PASS_TOKENS in one launch: a distinct expert is read once for all of
- * its tokens. */
+/* The per-slot calls run a pass above this many tokens as consecutive launches of equal size, up
+ * to 32 tokens when the workspace holds moe_workspace_bytes(layer, min(n, 32)), else up to this many
+ * (the per-slot form reads every slot's expert either way), so their workspace needs only
+ * moe_workspace_bytes(layer, MOE_PERSLOT_LAUNCH_TOKENS).  The deduplicating calls run a pass of
+ * up to MOE_MAX_PASS_TOKENS in one launch: a distinct expert is read once for all of its tokens. */
 #define MOE_PERSLOT_LAUNCH_TOKENS 16
 /* The per-slot calls' pass limit (the same as every call's). */
 #define MOE_MAX_PERSLOT_TOKENS 64
@@ -170,9 +170,10 @@ moe_status_t moe_group_slots(const int32_t *ids, int32_t n, int32_t m, int32_t N
  *   y     [dev] fp32 [n, d]    accumulate == 0: y is overwritten; != 0: added to.
  *   ws    [dev] workspace of ws_bytes >= moe_workspace_bytes(layer, n).
  * Supported: 1 <= n <= MOE_MAX_PASS_TOKENS.  A pass above MOE_PERSLOT_LAUNCH_TOKENS runs as
- * consecutive launches of up to MOE_PERSLOT_LAUNCH_TOKENS tokens on s (the per-slot form reads
- * every slot's expert either way; the launches write disjoint rows of y and share ws, which
- * needs only moe_workspace_bytes(layer, MOE_PERSLOT_LAUNCH_TOKENS)).  Each launch is validated
+ * consecutive launches on s of equal size, up to 32 tokens when ws_bytes >= moe_workspace_bytes(layer,
+ * min(n, 32)), else up to MOE_PERSLOT_LAUNCH_TOKENS (the per-slot form reads every slot's
+ * expert either way; the launches write disjoint rows of y and share ws, which needs only
+ * moe_workspace_bytes(layer, MOE_PERSLOT_LAUNCH_TOKENS)).  Each launch is validated
  * before it is enqueued and the first error ends the call; the chunks share the layer and
  * the pointers' alignment, so an argument error is found before the first launch.
  * Summation order inside y is not fixed (results may differ in the last bits between runs).

@@ -180,6 +180,18 @@ bool layer_uses_tc(const moe_layer_t *L) { return check_layer(L) == MOE_OK && us
 }  // namespace moe
 
 namespace {
+// Tokens per launch of a per-slot pass: the whole pass up to MOE_PERSLOT_LAUNCH_TOKENS; above,
+// launches of up to 32 (one launch of the 32-token kernel is faster than two of 16) when the
+// workspace holds that many, else of up to MOE_PERSLOT_LAUNCH_TOKENS, split evenly.  Passes are not
+// run as launches of 64: the 64-token kernel streams a per-slot pass more slowly than two of 32.
+int32_t perslot_launch_tokens(const moe_layer_t *L, int32_t n, size_t ws_bytes) {
+    if (n <= MOE_PERSLOT_LAUNCH_TOKENS) return n;
+    const int32_t wide = n < 32 ? n : 32;
+    const int32_t cap = ws_bytes >= moe_workspace_bytes(L, wide) ? wide : MOE_PERSLOT_LAUNCH_TOKENS;
+    const int32_t launches = (n + cap - 1) / cap;
+    return (n + launches - 1) / launches;   // equal launches (40 tokens: two of 20, not 32 and 8)
+}
+
 // Element size of a layer's activations (bf16, fp32 or e4m3).
 size_t x_elt_bytes(const moe_layer_t *L) { return L->x_dtype == MOE_BF16 ? 2u : (L->x_dtype == MOE_E4M3 ? 1u : 4u); }
 }  // namespace
@@ -256,14 +268,15 @@ moe_status_t moe_expert_op_perslot(const moe_layer_t *layer, const void *w_gate,
                                    moe_stream_t s) {
     moe_status_t st0 = check_perslot_call(layer, w_gate, w_up, w_down, x, ids, gates, n, y);
     if (st0 != MOE_OK) return st0;
-    if (n > MOE_PERSLOT_LAUNCH_TOKENS && n <= MOE_MAX_PASS_TOKENS) {
-        // consecutive launches of up to MOE_PERSLOT_LAUNCH_TOKENS tokens (each validates its part)
+    const int32_t cap = perslot_launch_tokens(layer, n, ws_bytes);
+    if (cap < n && n <= MOE_MAX_PASS_TOKENS) {
+        // consecutive launches of up to cap tokens (each validates its part)
         moe_status_t st = check_layer(layer);
         if (st != MOE_OK) return st;
         if (x == nullptr || ids == nullptr || gates == nullptr || y == nullptr) return MOE_ERR_ARG;
         const size_t xrow = static_cast<size_t>(layer->d) * x_elt_bytes(layer);
-        for (int32_t t0 = 0; t0 < n; t0 += MOE_PERSLOT_LAUNCH_TOKENS) {
-            const int32_t nc = n - t0 < MOE_PERSLOT_LAUNCH_TOKENS ? n - t0 : MOE_PERSLOT_LAUNCH_TOKENS;
+        for (int32_t t0 = 0; t0 < n; t0 += cap) {
+            const int32_t nc = n - t0 < cap ? n - t0 : cap;
             const size_t so = static_cast<size_t>(t0) * layer->m;
             st = moe_expert_op_perslot(layer, w_gate, w_up, w_down, static_cast<const uint8_t *>(x) + t0 * xrow,
                                        ids + so, gates + so, nc, accumulate, y + static_cast<size_t>(t0) * layer->d,
@@ -326,14 +339,15 @@ moe_status_t moe_expert_op_perslot_fp8(const moe_layer_t *layer, const void *w_g
                                        const void *w_down, const moe_weight_scales_t *scales, const void *x,
                                        const float *x_scale, const int32_t *ids, const float *gates, int32_t n,
                                        int32_t accumulate, float *y, void *ws, size_t ws_bytes, moe_stream_t s) {
-    if (n > MOE_PERSLOT_LAUNCH_TOKENS && n <= MOE_MAX_PASS_TOKENS) {
-        // consecutive launches of up to MOE_PERSLOT_LAUNCH_TOKENS tokens (each validates its part)
+    const int32_t cap = perslot_launch_tokens(layer, n, ws_bytes);
+    if (cap < n && n <= MOE_MAX_PASS_TOKENS) {
+        // consecutive launches of up to cap tokens (each validates its part)
         moe_status_t st = check_layer(layer);
         if (st != MOE_OK) return st;
         if (x == nullptr || x_scale == nullptr || ids == nullptr || gates == nullptr || y == nullptr) return MOE_ERR_ARG;
         const size_t xrow = static_cast<size_t>(layer->d) * x_elt_bytes(layer);
-        for (int32_t t0 = 0; t0 < n; t0 += MOE_PERSLOT_LAUNCH_TOKENS) {
-            const int32_t nc = n - t0 < MOE_PERSLOT_LAUNCH_TOKENS ? n - t0 : MOE_PERSLOT_LAUNCH_TOKENS;
+        for (int32_t t0 = 0; t0 < n; t0 += cap) {
+            const int32_t nc = n - t0 < cap ? n - t0 : cap;
             const size_t so = static_cast<size_t>(t0) * layer->m;
             st = moe_expert_op_perslot_fp8(layer, w_gate, w_up, w_down, scales,
                                            static_cast<const uint8_t *>(x) + t0 * xrow, x_scale + t0, ids + so,

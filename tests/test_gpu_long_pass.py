@@ -232,3 +232,32 @@ def test_largest_layer_dimensions(oracle_mod):
     rows = {t: oracle_mod.expert_op_token(*dl.host_experts(ids_h[t]), xh, local, g_h, t) for t in range(n)}
     _check_rows(ys, rows)
     _check_rows(yd, rows)
+
+
+@pytest.mark.parametrize("n", [17, 32, 33, 64])
+def test_perslot_long_pass_in_one_launch(oracle_mod, n):
+    """A per-slot pass above 16 tokens runs as equal launches of up to 32 tokens (the 32-token
+    form) when the workspace holds 32 tokens, and of up to 16 when it holds 16: the same result,
+    bf16 and e4m3, against the oracle.  The two agree to 2e-3 of the output's scale, not to the
+    last bit: launches of different sizes split each gate/up sum over CTAs differently, so its
+    fp32 shares add in another order and h's rounding to bf16 (e4m3) can differ by one step."""
+    d, f, N, m = 512, 256, 32, 8
+    dl = DeviceLayer(d, f, N, m, "bf16", seed=920 + n)
+    x = dl.activations(n, seed=921 + n)
+    _, logits = synth.routing_traces(1, n, N, m, 0.4, seed=922 + n)
+    ids, gates = route(logits[0], m)
+    ws_n, ws_16 = api.workspace(dl.layer, n, "cuda"), api.workspace(dl.layer, 16, "cuda")
+    y1 = api.expert_op_perslot(dl.layer, dl.w, x, ids, gates, ws=ws_n).cpu().numpy()
+    y2 = api.expert_op_perslot(dl.layer, dl.w, x, ids, gates, ws=ws_16).cpu().numpy()
+    assert api.last_device_error(ws_n) == 0 and api.last_device_error(ws_16) == 0
+    assert rel_max_err(y1, y2) <= 2e-3
+    ref = oracle_mod.expert_op_perslot(*dl.host(), synth.host_array(x), ids.cpu().numpy(), gates.cpu().numpy())
+    assert rel_max_err(y1, ref) <= TOL_BF16
+    l8 = api.make_layer(d, f, N, m, "e4m3")
+    w8, sc = api.quantize_experts(dl.w)
+    xq, sx = api.quantize_rows_e4m3(x)
+    w8n, w816 = api.workspace(l8, n, "cuda"), api.workspace(l8, 16, "cuda")
+    z1 = api.expert_op_perslot_fp8(l8, w8, sc, xq, sx, ids, gates, ws=w8n).cpu().numpy()
+    z2 = api.expert_op_perslot_fp8(l8, w8, sc, xq, sx, ids, gates, ws=w816).cpu().numpy()
+    assert api.last_device_error(w8n) == 0 and api.last_device_error(w816) == 0
+    assert rel_max_err(z1, z2) <= 2e-3
