@@ -66,7 +66,6 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kHWarps = kWarps - 6;           // h-former warps (6 ..)
 constexpr int kOB = 128;                      // d rows per down block
 constexpr uint32_t kWBytes = 16384;           // weight bytes of one block
-constexpr int kUnit = 2;                      // down blocks per TMEM accumulator (a unit)
 constexpr long long kDrainCycles = 400000000ll;   // about 0.2 s
 // the grouping of the deduplicating form from ids: expert list, offsets, slot order, the count,
 // two scan scratch rows, a copy of the ids (then the per-expert counts, N <= 1024)
@@ -123,31 +122,36 @@ struct Cfg<64> {
     using Mask = uint64_t;
 };
 
-// Shared memory of an instantiation: the ring, kHRing h entries, their run records, each
+// Shared memory of an instantiation (token width NT, U down blocks per TMEM accumulator, a
+// unit): the ring, kHRing h entries, their run records, each
 // epilogue warp's copy of the token scales (FP8) and of its run's gates, the token tables
 // of the wide form (below), then barriers full[S], empty[S], gacc_full[G], gacc_empty[G],
 // dacc_full[B], dacc_empty[B], h_full[R], h_empty[R], drain, the misc words, the in-kernel
 // grouping and the per-expert counts.
-template <int NT>
+template <int NT, int U>
 struct Lay : Cfg<NT> {
     using C = Cfg<NT>;
+    // units of 4 blocks take h entries twice as large: the 32-token form keeps 2 of them, the
+    // 64-token form one ring slot fewer
+    static constexpr int kStages = (NT == 64 && U == 4) ? C::kStages - 1 : C::kStages;
+    static constexpr int kHRing = (NT == 32 && U == 4) ? 2 : C::kHRing;
     static constexpr uint32_t kXTileBytes = NT * 128;   // x of one k slice: NT rows x 128 B
     static constexpr uint32_t kSlotBytes = kWBytes + kXTileBytes;   // gate/up block + x, or down block
     static constexpr uint32_t kHBytes = NT * 128;       // one h tile: NT rows x 128 B
-    static constexpr uint32_t kHEntry = kUnit * kHBytes;
+    static constexpr uint32_t kHEntry = U * kHBytes;
     // a run record: the token mask (2 words), the NT gates, the NT h scales (FP8)
     static constexpr uint32_t kInfoBytes = ((2 + 2 * NT) * 4 + 15) & ~15u;
     static constexpr uint32_t kDnCol0 = NT * C::kGuBufs;   // gate/up accumulators first, then down
-    static constexpr uint32_t kHOff = C::kStages * kSlotBytes;
-    static constexpr uint32_t kInfoOff = kHOff + C::kHRing * kHEntry;
-    static constexpr uint32_t kSxOff = kInfoOff + C::kHRing * kInfoBytes;
+    static constexpr uint32_t kHOff = kStages * kSlotBytes;
+    static constexpr uint32_t kInfoOff = kHOff + kHRing * kHEntry;
+    static constexpr uint32_t kSxOff = kInfoOff + kHRing * kInfoBytes;
     static constexpr uint32_t kGwOff = kSxOff + 4 * NT * 4;
     // wide form: slot positions and summed gates of the current group of each epilogue and
     // h-former warp (the 16-token form keeps them in registers)
     static constexpr uint32_t kTabOff = kGwOff + 4 * NT * 4;
     static constexpr uint32_t kTabBytes = NT == 16 ? 0u : 8u * NT * 8u;
     static constexpr uint32_t kBarOff = kTabOff + kTabBytes;
-    static constexpr int kNumBars = 2 * C::kStages + 2 * C::kGuBufs + 2 * C::kDownBufs + 2 * C::kHRing + 1;
+    static constexpr int kNumBars = 2 * kStages + 2 * C::kGuBufs + 2 * C::kDownBufs + 2 * kHRing + 1;
     static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr uint32_t kGrpOff = kMiscOff + 16;
     static constexpr uint32_t kCntOff = kGrpOff + ((kGrpWords * 4 + 15) & ~15u);
@@ -161,18 +165,23 @@ struct Lay : Cfg<NT> {
     static_assert(NT % 16 == 0 && NT <= 64 && sizeof(typename C::Mask) * 8 >= NT, "token width");
 };
 
-// Element type of a kernel instantiation: bf16 (kind::f16) or e4m3 (kind::f8f6f4).
-template <bool F8, int NT>
+// Element type of a kernel instantiation: bf16 (kind::f16) or e4m3 (kind::f8f6f4), with
+// token width NT and U down blocks per accumulator.
+template <bool F8, int NT, int U>
 struct Elt {
     static constexpr int BK = F8 ? 128 : 64;   // k elements per 128-byte row of an operand tile
     static constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(128, NT) : idesc_bf16_f32(128, NT);
     // a down block spans TPB 64-row gate/up tiles of f (one 128-byte row of W_down: 64 bf16 or
-    // 128 e4m3), a unit kUnit blocks, a down item ITEM tiles: 128 f (bf16) or 256 f (e4m3)
+    // 128 e4m3), a unit U blocks, a down item ITEM tiles: 128 or 256 f (bf16, U = 2 or 4), 256 f
+    // (e4m3, U = 2: the span of one h scale)
     static constexpr int TPB = F8 ? 2 : 1;
-    static constexpr int UNIT = kUnit;
-    static constexpr int ITEM = kUnit * TPB;
+    static constexpr int UNIT = U;
+    static constexpr int ITEM = U * TPB;
     static constexpr int COLS = ITEM * 64 / 32;   // f columns of an item per h-former lane
-    static constexpr int TK = F8 ? 1 : 2;         // tokens per round of the h formers' loads (64-bit tagged words)
+    // tokens per round of the h formers' loads: the 64-bit tagged words of 2 tokens fit the
+    // registers at 4 columns a lane, of 1 at 8
+    static constexpr int TK = COLS > 4 ? 1 : 2;
+    static_assert(!F8 || U == 2, "e4m3 items span 256 f, the h scale's block");
     __device__ __forceinline__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
         if constexpr (F8) tc_mma_f8(d, a, b, IDESC, acc);
         else tc_mma_bf16(d, a, b, IDESC, acc);
@@ -498,12 +507,12 @@ __device__ void build_grouping(const ExpertArgs &a, int my_id, int32_t *lst, int
 
 // ==================================================================== the kernel
 
-template <bool F8, int NT>
+template <bool F8, int NT, int U>
 __global__ void __launch_bounds__(kThreads, 1)
 expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
                  const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_x,
                  const ExpertArgs a, uint64_t *const part, const int zero_y) {
-    using L = Lay<NT>;
+    using L = Lay<NT, U>;
     using Mask = typename L::Mask;
     constexpr int kStages = L::kStages, kDownBufs = L::kDownBufs, kEpiBatch = L::kEpiBatch;
     constexpr int kHRing = L::kHRing, kGuBufs = L::kGuBufs;
@@ -642,7 +651,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         st_release_gpu(a.sync, ticket);
     }
 
-    using E = Elt<F8, NT>;
+    using E = Elt<F8, NT, U>;
     const int T = a.f / kFTile;
     const int KB = a.d / E::BK;
     const int G = num_groups(ar);
@@ -808,7 +817,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                     break;
                 }
                 tc_fence_after();
-                // the unit's blocks (at most E::UNIT = 2), in rounds as above
+                // the unit's blocks (at most E::UNIT), in rounds as above
                 for (int sub = s0; sub < s1;) {
                     const uint32_t st[2] = {cnt % kStages, (cnt + 1) % kStages};
                     if (!warp_wait(bar_full + 8u * st[0], (cnt / kStages) & 1u, abort_flag, a.err, wl)) {
@@ -1328,20 +1337,21 @@ bool encode_2d(CUtensorMap *map, const void *ptr, bool bytes1, uint64_t inner, u
 
 struct DeviceInfo {
     int sms = 0;
-    bool attr_set[6] = {false, false, false, false, false, false};   // (e4m3, token width)
+    bool attr_set[7] = {false, false, false, false, false, false, false};   // per kernel form
 };
 
 std::mutex g_info_mu;
 DeviceInfo g_info[64];
 
-template <bool F8, int NT>
+template <bool F8, int NT, int U>
 cudaError_t set_attributes() {
-    return cudaFuncSetAttribute(expert_tc_kernel<F8, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<NT>::kSmem);
+    return cudaFuncSetAttribute(expert_tc_kernel<F8, NT, U>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Lay<NT, U>::kSmem);
 }
 
-template <bool F8, int NT>
+template <bool F8, int NT, int U>
 cudaError_t launch(const ExpertArgs &a, int sms, int max_groups, bool zero_y, uint64_t *part, cudaStream_t s, bool pdl) {
-    using E = Elt<F8, NT>;
+    using E = Elt<F8, NT, U>;
     const long long T = a.f / kFTile, OBS = a.d / kOB;
     const long long T2 = (T + E::ITEM - 1) / E::ITEM;
     // CTAs with work: up to 2*G*T gate/up shares, and at most one per down block
@@ -1363,11 +1373,11 @@ cudaError_t launch(const ExpertArgs &a, int sms, int max_groups, bool zero_y, ui
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Lay<NT>::kSmem;
+    cfg.dynamicSmemBytes = Lay<NT, U>::kSmem;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, expert_tc_kernel<F8, NT>, tm_wg, tm_wu, tm_wd, tm_x, a, part, zero_y ? 1 : 0);
+    return cudaLaunchKernelEx(&cfg, expert_tc_kernel<F8, NT, U>, tm_wg, tm_wu, tm_wd, tm_x, a, part, zero_y ? 1 : 0);
 }
 
 }  // namespace
@@ -1385,9 +1395,13 @@ cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, u
     if (f8 && (a.d % 128 != 0 || a.f % 128 != 0 || a.s_gate == nullptr || a.s_up == nullptr ||
                a.s_down == nullptr || a.s_x == nullptr))
         return cudaErrorNotSupported;
-    // the token width: the narrowest instantiation that holds the pass
+    // the token width: the narrowest instantiation that holds the pass; the unit: 4 down blocks
+    // per accumulator (half the combine's reductions per y element) for bf16 per-slot launches,
+    // one-token passes and the wide forms, 2 for bf16 deduplicating passes of 2-16 tokens (their
+    // h formers take two tokens a round at 2-tile items) and for every e4m3 form
     const int width = a.n <= 16 ? 0 : (a.n <= 32 ? 1 : 2);
-    const int form = (f8 ? 1 : 0) + 2 * width;
+    const bool u4 = !f8 && (a.mode == kModePerSlot || a.n == 1 || width > 0);
+    const int form = f8 ? 4 + width : (width == 0 ? (u4 ? 1 : 0) : 1 + width);
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -1401,12 +1415,13 @@ cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, u
         }
         if (!di.attr_set[form]) {
             switch (form) {
-                case 0: err = set_attributes<false, 16>(); break;
-                case 1: err = set_attributes<true, 16>(); break;
-                case 2: err = set_attributes<false, 32>(); break;
-                case 3: err = set_attributes<true, 32>(); break;
-                case 4: err = set_attributes<false, 64>(); break;
-                default: err = set_attributes<true, 64>(); break;
+                case 0: err = set_attributes<false, 16, 2>(); break;
+                case 1: err = set_attributes<false, 16, 4>(); break;
+                case 2: err = set_attributes<false, 32, 4>(); break;
+                case 3: err = set_attributes<false, 64, 4>(); break;
+                case 4: err = set_attributes<true, 16, 2>(); break;
+                case 5: err = set_attributes<true, 32, 2>(); break;
+                default: err = set_attributes<true, 64, 2>(); break;
             }
             if (err != cudaSuccess) return err;
             di.attr_set[form] = true;
@@ -1414,12 +1429,13 @@ cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, u
         sms = di.sms;
     }
     switch (form) {
-        case 0: return launch<false, 16>(a, sms, max_groups, zero_y, part, s, pdl);
-        case 1: return launch<true, 16>(a, sms, max_groups, zero_y, part, s, pdl);
-        case 2: return launch<false, 32>(a, sms, max_groups, zero_y, part, s, pdl);
-        case 3: return launch<true, 32>(a, sms, max_groups, zero_y, part, s, pdl);
-        case 4: return launch<false, 64>(a, sms, max_groups, zero_y, part, s, pdl);
-        default: return launch<true, 64>(a, sms, max_groups, zero_y, part, s, pdl);
+        case 0: return launch<false, 16, 2>(a, sms, max_groups, zero_y, part, s, pdl);
+        case 1: return launch<false, 16, 4>(a, sms, max_groups, zero_y, part, s, pdl);
+        case 2: return launch<false, 32, 4>(a, sms, max_groups, zero_y, part, s, pdl);
+        case 3: return launch<false, 64, 4>(a, sms, max_groups, zero_y, part, s, pdl);
+        case 4: return launch<true, 16, 2>(a, sms, max_groups, zero_y, part, s, pdl);
+        case 5: return launch<true, 32, 2>(a, sms, max_groups, zero_y, part, s, pdl);
+        default: return launch<true, 64, 2>(a, sms, max_groups, zero_y, part, s, pdl);
     }
 }
 
