@@ -819,18 +819,24 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 tc_fence_after();
                 // the unit's blocks (at most E::UNIT), in rounds as above
                 for (int sub = s0; sub < s1;) {
-                    const uint32_t st[2] = {cnt % kStages, (cnt + 1) % kStages};
-                    if (!warp_wait(bar_full + 8u * st[0], (cnt / kStages) & 1u, abort_flag, a.err, wl)) {
+                    if (!warp_wait(bar_full + 8u * (cnt % kStages), (cnt / kStages) & 1u, abort_flag, a.err, wl)) {
                         ok = false;
                         break;
                     }
-                    const int nbk = (s1 - sub >= 2 && __all_sync(kFull, mbar_test_wait(bar_full + 8u * st[1],
-                                                                                      ((cnt + 1) / kStages) & 1u)))
-                                        ? 2 : 1;
+                    // the unit's next blocks join the round while their copies have landed
+                    int nbk = 1;
+#pragma unroll
+                    for (int j = 1; j < E::UNIT; ++j)
+                        if (nbk == j && s1 - sub > j &&
+                            __all_sync(kFull, mbar_test_wait(bar_full + 8u * ((cnt + j) % kStages), ((cnt + j) / kStages) & 1u)))
+                            nbk = j + 1;
+                    uint32_t st[E::UNIT];
+#pragma unroll
+                    for (int j = 0; j < E::UNIT; ++j) st[j] = (cnt + j) % kStages;
                     tc_fence_after();
                     if (elect_one()) {
 #pragma unroll
-                        for (int j = 0; j < 2; ++j) {
+                        for (int j = 0; j < E::UNIT; ++j) {
                             if (j >= nbk) break;
                             const uint32_t sa = base + st[j] * kSlotBytes;
                             const uint32_t sbs = shb + static_cast<uint32_t>(sub + j) * kHBytes;
