@@ -9,10 +9,11 @@
 // other byte off the memory path.
 //
 // A group is one slot (per-slot form) or one distinct expert with all of its tokens
-// (deduplicating form).  One call is one persistent kernel, one CTA per SM, 10 warps:
-// warp 0 the TMA producer, warp 1 the tcgen05.mma issuer, warps 2-5 the epilogue (one TMEM
-// lane per thread), warps 6-9 the h formers.  Every CTA streams its share of two block
-// lists through one ring of shared-memory slots, without a break between them:
+// (deduplicating form).  One call is one persistent kernel, one CTA per SM, 11 warps:
+// warp 0 the TMA producer, warp 1 the tcgen05.mma issuer (with down units of four blocks,
+// warp 10 a second one for every other down unit), warps 2-5 the epilogue (one TMEM lane per
+// thread), warps 6-9 the h formers.  Every CTA streams its share of two block lists through one
+// ring of shared-memory slots, without a break between them:
 //
 //   gate/up blocks.  A gate/up item is (group, 64-row tile of f); its block is one k slice:
 //   64 rows of W_gate and the same 64 rows of W_up (16 KB, the M = 128 operand) plus the
@@ -61,9 +62,11 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 320;                 // warps: producer, MMA, 4 epilogue, 4 h formers
+// warps: producer, MMA, 4 epilogue, 4 h formers, a second MMA issuer for the down phase
+constexpr int kThreads = 352;
 constexpr int kWarps = kThreads / 32;
-constexpr int kHWarps = kWarps - 6;           // h-former warps (6 ..)
+constexpr int kHWarps = 4;                    // h-former warps (6 .. 9)
+constexpr int kMma2Warp = 10;                 // issues every other down unit of 4-block units
 constexpr int kOB = 128;                      // d rows per down block
 constexpr uint32_t kWBytes = 16384;           // weight bytes of one block
 constexpr long long kDrainCycles = 400000000ll;   // about 0.2 s
@@ -126,8 +129,8 @@ struct Cfg<64> {
 // unit): the ring, kHRing h entries, their run records, each
 // epilogue warp's copy of the token scales (FP8) and of its run's gates, the token tables
 // of the wide form (below), then barriers full[S], empty[S], gacc_full[G], gacc_empty[G],
-// dacc_full[B], dacc_empty[B], h_full[R], h_empty[R], drain, the misc words, the in-kernel
-// grouping and the per-expert counts.
+// dacc_full[B], dacc_empty[B], h_full[R], h_empty[R], drain[2], the misc words, the ring slots'
+// block records, the in-kernel grouping and the per-expert counts.
 template <int NT, int U>
 struct Lay : Cfg<NT> {
     using C = Cfg<NT>;
@@ -151,9 +154,10 @@ struct Lay : Cfg<NT> {
     static constexpr uint32_t kTabOff = kGwOff + 4 * NT * 4;
     static constexpr uint32_t kTabBytes = NT == 16 ? 0u : 8u * NT * 8u;
     static constexpr uint32_t kBarOff = kTabOff + kTabBytes;
-    static constexpr int kNumBars = 2 * kStages + 2 * C::kGuBufs + 2 * C::kDownBufs + 2 * kHRing + 1;
+    static constexpr int kNumBars = 2 * kStages + 2 * C::kGuBufs + 2 * C::kDownBufs + 2 * kHRing + 2;
     static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
-    static constexpr uint32_t kGrpOff = kMiscOff + 16;
+    static constexpr uint32_t kRecOff = kMiscOff + 16;   // the block each ring slot last received
+    static constexpr uint32_t kGrpOff = kRecOff + ((4 * kStages + 15) & ~15u);
     static constexpr uint32_t kCntOff = kGrpOff + ((kGrpWords * 4 + 15) & ~15u);
     static constexpr uint32_t kSmem = kCntOff + 1024 * 4 + 1024;   // + alignment slack of the base
     static_assert(kSlotBytes % 1024 == 0 && kHOff % 1024 == 0 && kHEntry % 1024 == 0, "128-byte swizzle atoms");
@@ -162,6 +166,9 @@ struct Lay : Cfg<NT> {
     static_assert(4 * kThreads >= 1024 && kThreads >= kMaxFusedSlots && kHWarps >= 1 && kHWarps <= NT,
                   "grouping bins and slots, h-former warps");
     static_assert(kDnCol0 + NT * C::kDownBufs <= C::kTmemCols, "TMEM columns");
+    // units alternate between the two MMA issuers: with an even count every down accumulator
+    // belongs to one issuer, whose waits on it then follow each other phase by phase
+    static_assert(C::kDownBufs % 2 == 0, "down accumulators per issuer");
     static_assert(NT % 16 == 0 && NT <= 64 && sizeof(typename C::Mask) * 8 >= NT, "token width");
 };
 
@@ -505,6 +512,25 @@ __device__ void build_grouping(const ExpertArgs &a, int my_id, int32_t *lst, int
     if (warp >= 2) named_barrier(3, kThreads - 64);
 }
 
+// Bounded warp-wide wait until the shared word *p holds v: the same abort and time-limit rules
+// as mbar_wait, and the outcome is warp-uniform.
+__device__ __forceinline__ bool warp_wait_word(const volatile uint32_t *p, uint32_t v, volatile int32_t *abort,
+                                               int32_t *err, long long limit) {
+    if (__all_sync(kFull, *p == v)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (__all_sync(kFull, *p == v)) return true;
+        const bool late = clock64() - t0 > limit;
+        if (__any_sync(kFull, late || *abort != 0)) {
+            if (late && (threadIdx.x & 31) == 0) {
+                *abort = 1;
+                record_error(err, MOE_ERR_DEVICE_TIMEOUT);
+            }
+            return false;
+        }
+    }
+}
+
 // ==================================================================== the kernel
 
 template <bool F8, int NT, int U>
@@ -515,6 +541,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     using L = Lay<NT, U>;
     using Mask = typename L::Mask;
     constexpr int kStages = L::kStages, kDownBufs = L::kDownBufs, kEpiBatch = L::kEpiBatch;
+    constexpr int kIssuers = U == 4 ? 2 : 1;   // MMA issuers of the down phase
     constexpr int kHRing = L::kHRing, kGuBufs = L::kGuBufs;
     constexpr uint32_t kSlotBytes = L::kSlotBytes, kHBytes = L::kHBytes, kHEntry = L::kHEntry;
     constexpr uint32_t kInfoBytes = L::kInfoBytes, kDnCol0 = L::kDnCol0, kTmemCols = L::kTmemCols;
@@ -539,6 +566,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     const uint32_t bar_drain = bar_h_empty + 8u * kHRing;
     uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + kMiscOff);
     volatile int32_t *const abort_flag = reinterpret_cast<volatile int32_t *>(base_ptr + kMiscOff + 4);
+    volatile uint32_t *const slot_rec = reinterpret_cast<volatile uint32_t *>(base_ptr + L::kRecOff);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -560,9 +588,11 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         }
         for (int b = 0; b < kHRing; ++b) {
             mbar_init(bar_h_full + 8u * b, kHWarps);    // the run's leader for kHWarps - W + 1, each helper 1
-            mbar_init(bar_h_empty + 8u * b, 1 + 4);     // the MMAs' commit and the epilogue warps
+            mbar_init(bar_h_empty + 8u * b, kIssuers + 4);   // the MMA issuers' commits and the epilogue warps
         }
         mbar_init(bar_drain, 1);
+        mbar_init(bar_drain + 8u, 1);
+        for (int s = 0; s < kStages; ++s) slot_rec[s] = ~0u;
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_map(&tm_wg);
@@ -589,9 +619,9 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         prefetch_l2_range(a.gates, static_cast<size_t>(S) * 4, tid, kThreads);
         prefetch_l2_range(a.x, xb, tid, kThreads);
         if (a.mode == kModeDedup) {   // the grouping's buffer sizes, as the host validated them
-            const int U = S < a.N ? S : a.N;
-            prefetch_l2_range(a.expert_list, static_cast<size_t>(U) * 4, tid, kThreads);
-            prefetch_l2_range(a.offsets, static_cast<size_t>(U + 1) * 4, tid, kThreads);
+            const int nd = S < a.N ? S : a.N;   // at most this many distinct experts
+            prefetch_l2_range(a.expert_list, static_cast<size_t>(nd) * 4, tid, kThreads);
+            prefetch_l2_range(a.offsets, static_cast<size_t>(nd + 1) * 4, tid, kThreads);
             prefetch_l2_range(a.slot_order, static_cast<size_t>(S) * 4, tid, kThreads);
         }
     }
@@ -732,6 +762,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                     }
                     if (elect_one()) {
                         const uint32_t fb = bar_full + 8u * st;
+                        if (kIssuers == 2) slot_rec[st] = cnt;   // before the phase of block cnt can complete
                         mbar_arrive_expect_tx(fb, kWBytes);
                         tma_load_2d(base + st * kSlotBytes, &tm_wd, fb, (sg.tile * E::ITEM + sub * E::TPB) * kFTile,
                                     sg.e * a.d + ob * kOB);
@@ -743,16 +774,28 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         }
         prod_cnt = cnt;
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // Warp-uniform loop; waits by every lane, MMAs and commits by one elected lane.  A
+    } else if (warp == 1 || (kIssuers == 2 && warp == kMma2Warp)) {
+        // ------------------------------------------------------------ MMA issuers
+        // Warp-uniform loops; waits by every lane, MMAs and commits by one elected lane.  A
         // round of waits and issue costs about as much as four MMAs of its own, so a round
         // takes the next block of the same accumulator as well when its copy has already landed
         // (a non-blocking test): eight MMAs back to back where the stream runs ahead of the
-        // issuer, and no wait added where the issuer waits for the stream.
+        // issuer, and no wait added where the issuer waits for the stream.  Warp 1 issues the
+        // gate/up blocks.  With units of four blocks the down units alternate between warp 1 and
+        // warp 10 (each into its own accumulators), so two issuers feed the down phase; with
+        // units of two warp 1 issues them all (two issuers were no faster there).
+        const uint32_t mw = warp == 1 ? 0u : 1u;   // this issuer's down units: dcnt % 2 == mw
         uint32_t cnt = 0, seg = 0;
         bool ok = true;
-        for (long long b = glo; ok && b < ghi;) {
+        if (mw == 1u) {
+            // the down blocks follow this CTA's gate/up blocks in the ring
+            for (long long b = glo; b < ghi;) {
+                const Seg s = seg_at(ar, b, ghi, KB, T);
+                b = s.b1;
+                if (s.valid) cnt += static_cast<uint32_t>(s.b1 - s.b0);
+            }
+        }
+        for (long long b = glo; mw == 0u && ok && b < ghi;) {
             const Seg s = seg_at(ar, b, ghi, KB, T);
             b = s.b1;
             if (!s.valid) continue;
@@ -810,16 +853,24 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             for (int ob = u.ob_first(); ok && ob <= u.ob_last(); ++ob) {
                 const int s0 = u.s_lo(ob), s1 = u.s_hi(ob);
                 if (s0 >= s1) continue;
-                const uint32_t buf = dcnt % kDownBufs, dph = (dcnt / kDownBufs) & 1u;
-                ++dcnt;
+                const uint32_t du = dcnt++;
+                if (kIssuers == 2 && (du & 1u) != mw) {   // the other issuer's unit: its blocks pass by
+                    cnt += static_cast<uint32_t>(s1 - s0);
+                    continue;
+                }
+                const uint32_t buf = du % kDownBufs, dph = (du / kDownBufs) & 1u;
                 if (!warp_wait(bar_dacc_empty + 8u * buf, dph ^ 1u, abort_flag, a.err, wl)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // the unit's blocks (at most E::UNIT), in rounds as above
+                // The unit's blocks (at most E::UNIT), in rounds as above.  Each issuer skips the
+                // other's blocks, so the copy into a slot that precedes this block's may not have
+                // been issued yet, and a parity wait would then take that earlier phase for this
+                // block's: the wait starts once the producer has recorded this block in the slot.
                 for (int sub = s0; sub < s1;) {
-                    if (!warp_wait(bar_full + 8u * (cnt % kStages), (cnt / kStages) & 1u, abort_flag, a.err, wl)) {
+                    if ((kIssuers == 2 && !warp_wait_word(slot_rec + cnt % kStages, cnt, abort_flag, a.err, wl)) ||
+                        !warp_wait(bar_full + 8u * (cnt % kStages), (cnt / kStages) & 1u, abort_flag, a.err, wl)) {
                         ok = false;
                         break;
                     }
@@ -828,7 +879,8 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
 #pragma unroll
                     for (int j = 1; j < E::UNIT; ++j)
                         if (nbk == j && s1 - sub > j &&
-                            __all_sync(kFull, mbar_test_wait(bar_full + 8u * ((cnt + j) % kStages), ((cnt + j) / kStages) & 1u)))
+                            __all_sync(kFull, (kIssuers == 1 || slot_rec[(cnt + j) % kStages] == cnt + j) &&
+                                                  mbar_test_wait(bar_full + 8u * ((cnt + j) % kStages), ((cnt + j) / kStages) & 1u)))
                             nbk = j + 1;
                     uint32_t st[E::UNIT];
 #pragma unroll
@@ -859,10 +911,12 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         }
         // every MMA this warp issued completes before TMEM is released
         if (elect_one()) {
-            tc_commit(bar_drain);
-            mbar_wait_drain(bar_drain, 0, kDrainCycles);
+            tc_commit(bar_drain + 8u * mw);
+            mbar_wait_drain(bar_drain + 8u * mw, 0, kDrainCycles);
         }
         __syncwarp();
+    } else if (warp == kMma2Warp) {
+        // no second issuer in this form
     } else if (warp < 6) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;               // TMEM lane quarter of this warp
