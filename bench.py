@@ -76,8 +76,8 @@ def parse():
                    help="skip the page-shaped single-layer workloads (DeepSeek-V2-Lite, Qwen3, Mixtral at each reuse)")
     p.add_argument("--no-long", action="store_true", help="skip the passes of 17..64 tokens")
     p.add_argument("--profile-layer", default=None,
-                   help="comma-separated pass sizes: two deduplicating calls each on one layer of the workload's "
-                        "shape (a small case for ncu captures; prints ok)")
+                   help="comma-separated pass sizes, each n (two deduplicating calls from ids) or sn (two per-slot "
+                        "calls), on one layer of the workload's shape (a small case for ncu captures; prints ok)")
     p.add_argument("--long-only", action="store_true",
                    help="only the passes of 17..64 tokens on 8 freshly generated layers (prints their JSON)")
     p.add_argument("--configs-only", default=None,
@@ -957,22 +957,28 @@ def long_pass_leg(wl, weights, device, warmup: int = 2, steps: int = 3):
     return out
 
 
-def profile_layer(wl, ns):
+def profile_layer(wl, cases):
     """A small case for Nsight Compute: one layer of the workload's shape (1.2 GB of bf16 weights for
-    the Qwen3 shape, larger than L2), the reuse-0.4 routing of a pass of each size n, and two
-    deduplicating calls from ids per n on a workspace for 64 tokens."""
+    the Qwen3 shape, larger than L2), the reuse-0.4 routing of a pass of each size n, and two calls
+    per case on a workspace for the largest n: "n" the deduplicating call from ids, "sn" the
+    per-slot call (n <= 16: one launch)."""
     mbuild.build()
     device = torch.device("cuda", 0)
     layer = api.make_layer(wl.d, wl.f, wl.N, wl.m, "bf16")
     w = synth.expert_weights(wl.N, wl.f, wl.d, torch.bfloat16, 11, device=device)
-    ws = api.workspace(layer, max(ns), device)
-    x_all = synth.activations(max(ns), wl.d, torch.bfloat16, 2, device=device)
-    for n in ns:
+    parsed = [(c.startswith("s"), int(c.lstrip("s"))) for c in cases]
+    n_max = max(n for _, n in parsed)
+    ws = api.workspace(layer, n_max, device)
+    x_all = synth.activations(n_max, wl.d, torch.bfloat16, 2, device=device)
+    for perslot, n in parsed:
         _, logits = synth.routing_traces(1, n, wl.N, wl.m, 0.4, seed=3)
         ids, gates = api.route_topm(torch.from_numpy(logits[0]).to(device), wl.m)
         x = x_all[:n].contiguous()
         for _ in range(2):
-            api.expert_op_dedup_ids(layer, w, x, ids, gates, ws=ws)
+            if perslot:
+                api.expert_op_perslot(layer, w, x, ids, gates, ws=ws)
+            else:
+                api.expert_op_dedup_ids(layer, w, x, ids, gates, ws=ws)
         torch.cuda.synchronize(device)
     assert api.last_device_error(ws) == 0
     print("ok", flush=True)
@@ -1131,7 +1137,7 @@ def main():
         print(json.dumps(dict(configs=configs_leg(device, names=args.configs_only.split(",")))), flush=True)
         return
     if args.profile_layer:
-        profile_layer(BY_NAME[args.workload], [int(v) for v in args.profile_layer.split(",")])
+        profile_layer(BY_NAME[args.workload], args.profile_layer.split(","))
         return
     if args.long_only:
         mbuild.build()
