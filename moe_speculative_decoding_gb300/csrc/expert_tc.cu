@@ -1124,9 +1124,12 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         // ------------------------------------------------------------ h formers
         // The kHWarps warps take every run, up to kHRing runs ahead of the MMAs.  A run of a
         // group of cnt slots is formed by W = min(kHWarps, ceil(cnt / E::TK)) of them, from the
-        // run's leader (warp run % kHWarps) on, the k-th token (ascending) by the (k % W)-th:
-        // one round of loads per warp for small groups, the rounds of a large group spread over
-        // the warps, and consecutive runs led by different warps.  The other warps skip the
+        // run's leader on, the k-th token (ascending) by the (k % W)-th: one round of loads per
+        // warp for small groups, the rounds of a large group spread over the warps.  The leaders
+        // rotate by the warps each run takes (run r + 1 is led by the warp after run r's last
+        // one), so consecutive runs of small groups go to different warps and are formed side
+        // by side, and any kHWarps consecutive runs still give every warp a part, which keeps
+        // the h ring's parity waits exact (see Cfg).  The other warps skip the
         // run: the leader arrives for them on h_full (kHWarps - W + 1 arrivals, each helper
         // one), so none waits for a ring entry it does not fill.  W comes from the group's slot
         // count, which the h formers copy to shared memory first (1 per group in the per-slot
@@ -1150,7 +1153,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             gi.pos = tab;
             gi.gt = reinterpret_cast<float *>(tab + NT);
         }
-        uint32_t run = 0;
+        uint32_t run = 0, lead = 0;   // lead: warps taken by the earlier runs
         for (long long b = dlo; b < dhi;) {
             const Seg sg = seg_at(ar, b, dhi, IB, T2);
             b = sg.b1;
@@ -1159,7 +1162,8 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             const uint32_t hb = rr % kHRing, hph = (rr / kHRing) & 1u;
             const int cnt = ar.mode == kModePerSlot ? 1 : gcnt[sg.g];
             const int nw = min(kHWarps, max(1, (cnt + E::TK - 1) / E::TK));   // warps forming the run
-            const int first = (hw - static_cast<int>(rr % kHWarps) + kHWarps) % kHWarps;   // this warp's first token
+            const int first = (hw - static_cast<int>(lead % kHWarps) + kHWarps) % kHWarps;   // this warp's first token
+            lead += static_cast<uint32_t>(nw);
             if (first >= nw) {   // not a warp of this run
                 if constexpr (kHRing < kHWarps) {
                     // the entry's release in order with the others (see Cfg)
