@@ -83,13 +83,19 @@ constexpr uint32_t kGrpWords = 3 * kMaxFusedSlots + 1 + 1 + 2 * kWarps + kMaxFus
 // the memory latency at the stream's rate.
 //
 // The h ring needs no entry per h-former warp.  Its producers are kHWarps warps that each
-// form only some runs, so with fewer entries than warps a warp that waited only for its own
-// runs could pass an entry's parity wait a whole phase early (its last wait ordered it after
-// the release of run r' - kHRing with r' >= r - kHWarps, while the wait for run r is exact
-// only after the release of run r - 2 * kHRing).  A form with kHRing < kHWarps therefore
-// has every h-former warp wait for every run's entry in order, also for the runs it skips:
-// each wait then follows the one a phase before it, and none costs more than the entry's
-// reuse requires anyway.
+// form only some runs, and a warp forming run r first waits, with a parity wait, for the
+// release of run r - kHRing from its entry.  That wait is exact once run r - 2 * kHRing is
+// released (the entry is then at most one phase behind; it cannot be ahead, as run r is not
+// formed yet).  A warp knows that from its own last wait when it took part in one of the
+// kHRing runs before r; any kHWarps consecutive runs give every warp a part, so with
+// kHRing >= kHWarps that always holds.  With fewer entries than warps it need not (a warp
+// relying on its own waits alone could pass a whole phase early), so those forms keep a shared
+// count of the runs known to be released: every warp that passes an entry's wait for run r
+// raises it to r - kHRing + 1, and a warp waits for it to cover run r - 2 * kHRing before its
+// parity wait for run r.  Releases complete in run order (each issuer's commit covers all its
+// earlier MMAs, and the epilogue warps arrive run by run), so one seen release implies all
+// earlier ones.  (Waiting for every run's entry in order, also for the runs a warp skips, is
+// not enough: a skipping warp can fall behind an entry that others have released twice.)
 template <int NT>
 struct Cfg;
 template <>
@@ -531,6 +537,26 @@ __device__ __forceinline__ bool warp_wait_word(const volatile uint32_t *p, uint3
     }
 }
 
+// Bounded warp-wide wait until the shared count *p is at least v (it only grows): the same
+// abort and time-limit rules as mbar_wait, and the outcome is warp-uniform.
+__device__ __forceinline__ bool warp_wait_at_least(const uint32_t *p, uint32_t v, volatile int32_t *abort,
+                                                   int32_t *err, long long limit) {
+    const volatile uint32_t *const q = p;
+    if (__all_sync(kFull, *q >= v)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (__all_sync(kFull, *q >= v)) return true;
+        const bool late = clock64() - t0 > limit;
+        if (__any_sync(kFull, late || *abort != 0)) {
+            if (late && (threadIdx.x & 31) == 0) {
+                *abort = 1;
+                record_error(err, MOE_ERR_DEVICE_TIMEOUT);
+            }
+            return false;
+        }
+    }
+}
+
 // ==================================================================== the kernel
 
 template <bool F8, int NT, int U>
@@ -566,6 +592,8 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
     const uint32_t bar_drain = bar_h_empty + 8u * kHRing;
     uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(base_ptr + kMiscOff);
     volatile int32_t *const abort_flag = reinterpret_cast<volatile int32_t *>(base_ptr + kMiscOff + 4);
+    // runs below this are known to be released from the h ring (forms with kHRing < kHWarps)
+    uint32_t *const h_seen = reinterpret_cast<uint32_t *>(base_ptr + kMiscOff + 8);
     volatile uint32_t *const slot_rec = reinterpret_cast<volatile uint32_t *>(base_ptr + L::kRecOff);
 
     const int warp = threadIdx.x >> 5;
@@ -593,6 +621,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
         mbar_init(bar_drain, 1);
         mbar_init(bar_drain + 8u, 1);
         for (int s = 0; s < kStages; ++s) slot_rec[s] = ~0u;
+        *h_seen = 0u;
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_map(&tm_wg);
@@ -1164,13 +1193,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
             const int nw = min(kHWarps, max(1, (cnt + E::TK - 1) / E::TK));   // warps forming the run
             const int first = (hw - static_cast<int>(lead % kHWarps) + kHWarps) % kHWarps;   // this warp's first token
             lead += static_cast<uint32_t>(nw);
-            if (first >= nw) {   // not a warp of this run
-                if constexpr (kHRing < kHWarps) {
-                    // the entry's release in order with the others (see Cfg)
-                    if (!warp_wait(bar_h_empty + 8u * hb, hph ^ 1u, abort_flag, a.err, wl)) break;
-                }
-                continue;
-            }
+            if (first >= nw) continue;   // not a warp of this run
             group_tokens(ar, sg.g, lane, gi);
             // this warp's tokens: every nw-th of the group's, from its first
             Mask mymask = gi.mask;
@@ -1204,8 +1227,18 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constan
                 p0[tl] = gsp.part_of(first);
                 span[tl] = min(gsp.part_of(first + KB - 1) - p0[tl] + 1, kMaxSpan);
             }
-            // a warp arrives for a run only after its entry is free, so no arrival runs ahead
+            // a warp arrives for a run only after its entry is free, so no arrival runs ahead;
+            // with fewer entries than warps, the parity wait follows a seen release of run
+            // rr - 2 kHRing (see Cfg)
+            if constexpr (kHRing < kHWarps) {
+                if (rr >= 2u * kHRing &&
+                    !warp_wait_at_least(h_seen, rr - 2u * kHRing + 1u, abort_flag, a.err, wl))
+                    break;
+            }
             if (!warp_wait(bar_h_empty + 8u * hb, hph ^ 1u, abort_flag, a.err, wl)) break;
+            if constexpr (kHRing < kHWarps) {
+                if (lane == 0 && rr >= static_cast<uint32_t>(kHRing)) atomicMax(h_seen, rr - kHRing + 1u);
+            }
             bool parts_ok = true;
             uint8_t *const hp = h_ptr + hb * kHEntry;
             uint32_t *const rec = reinterpret_cast<uint32_t *>(info_ptr + hb * kInfoBytes);
