@@ -1494,10 +1494,11 @@ cudaError_t launch_expert_tc(const ExpertArgs &a, int max_groups, bool zero_y, u
         return cudaErrorNotSupported;
     // the token width: the narrowest instantiation that holds the pass; the unit: 4 down blocks
     // per accumulator (half the combine's reductions per y element) for bf16 per-slot launches,
-    // one-token passes and the wide forms, 2 for bf16 deduplicating passes of 2-16 tokens (their
-    // h formers take two tokens a round at 2-tile items) and for every e4m3 form
+    // deduplicating passes of 1-2 and of 12 or more tokens and the wide forms, 2 for bf16
+    // deduplicating passes of 3-11 tokens (their h formers take two tokens a round at 2-tile
+    // items, which measured faster there) and for every e4m3 form
     const int width = a.n <= 16 ? 0 : (a.n <= 32 ? 1 : 2);
-    const bool u4 = !f8 && (a.mode == kModePerSlot || a.n == 1 || width > 0);
+    const bool u4 = !f8 && (a.mode == kModePerSlot || a.n <= 2 || a.n >= 12 || width > 0);
     const int form = f8 ? 4 + width : (width == 0 ? (u4 ? 1 : 0) : 1 + width);
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
