@@ -24,6 +24,9 @@ find the failure when the safeguard is taken away, so that it is able to see one
    kernel keeps a shared count of the runs seen released and waits for it first; waiting for
    every run's entry in order, also for the runs a warp skips, can deadlock (a skipping warp
    falls two phases behind an entry that other warps keep releasing).
+
+3. The down accumulators with two issuers: units alternate between the issuers and cycle
+   through B accumulators; the epilogue reads them in order.
 """
 import numpy as np
 import pytest
@@ -231,3 +234,63 @@ def test_h_ring_with_fewer_entries_uses_the_released_count():
 @pytest.mark.parametrize("R,H", [(1, 4), (3, 4), (4, 5), (2, 5)])
 def test_h_ring_released_count_is_exact_for_any_ring(R, H):
     assert hring_violations(R, H, rotate=True, in_order=False, seen=True) == 0
+
+
+def dacc_run(rng, B, units):
+    """One random interleaving of the down accumulators with two issuers: unit u goes to issuer
+    u % 2 and to accumulator u % B; an issuer waits for its accumulator's release by the unit B
+    before (`dacc_empty`), fills it and commits `dacc_full`; the epilogue takes the units in
+    order.  Returns the first violation (the epilogue reading an accumulator that does not hold
+    its unit, or an issuer overwriting one the epilogue has not read), or None."""
+    full = [Barrier() for _ in range(B)]
+    empty = [Barrier() for _ in range(B)]
+    content = [None] * B
+    read = [False] * units
+    mine = [[u for u in range(units) if u % 2 == i] for i in range(2)]
+    pos = [0, 0]
+    epi = 0
+    filling = []        # MMAs in flight: (accumulator, unit)
+    while True:
+        acts = []
+        for i in (0, 1):
+            if pos[i] < len(mine[i]):
+                u = mine[i][pos[i]]
+                if empty[u % B].passes(((u // B) & 1) ^ 1):
+                    acts.append(("issue", i))
+        if filling:
+            acts.append(("complete", None))
+        if epi < units and full[epi % B].passes((epi // B) & 1):
+            acts.append(("read", None))
+        if not acts:
+            return None if epi == units else ("deadlock", epi)
+        kind, i = acts[rng.integers(len(acts))]
+        if kind == "issue":
+            u = mine[i][pos[i]]
+            if u >= B and not read[u - B]:
+                return ("overwrite", u)
+            filling.append((u % B, u))
+            pos[i] += 1
+        elif kind == "complete":
+            b, u = filling.pop(rng.integers(len(filling)))
+            content[b] = u
+            full[b].arrive()
+        else:
+            b = epi % B
+            if content[b] != epi:
+                return ("read", epi, content[b])
+            read[epi] = True
+            empty[b].arrive()
+            epi += 1
+
+
+def test_down_accumulators_with_two_issuers():
+    """With an even number of accumulators (8 or 6 in the kernel, which requires an even count)
+    each belongs to one issuer, whose waits on it follow each other phase by phase.  Odd counts
+    from 3 are exact as well (an issuer's unit between two uses of an accumulator waits on
+    another one, whose release by the in-order epilogue implies the earlier release), but a
+    single accumulator shared by both issuers is not: the model finds an issuer overwriting a
+    unit the epilogue has not read."""
+    rng = np.random.default_rng(3)
+    for B in (6, 8, 3, 5):
+        assert all(dacc_run(rng, B, int(rng.integers(4, 60))) is None for _ in range(300))
+    assert any(dacc_run(rng, 1, int(rng.integers(4, 30))) is not None for _ in range(300))
